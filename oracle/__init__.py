@@ -1,0 +1,158 @@
+"""CPU oracle for MoE token dispatch + expert GEMM. TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline
+and reference legs may import this package. The product path (the
+``moe_token_dispatch_gb300`` package and its CUDA library) never imports,
+links or calls it, and shares no code with it.
+
+The arithmetic lives in ``oracle.c`` (plain C, float64); this module only
+marshals numpy arrays. What each step computes, following the expert-parallel
+"token-dispatch + GEMM" of "Loads and Loads of Fluffy Kittens" (section "Key
+claims", Fig. 17) restated for one device:
+
+* ``route_counts``  -- tokens routed to each expert, and the exclusive
+  prefix sum of those counts (``offsets[E] == T*k``);
+* ``build_perm``    -- flat routing indices ``t*k+s`` grouped by expert, in
+  increasing ``t*k+s`` inside each expert; and its inverse;
+* ``gemm_rows``     -- for sorted row ``j`` of expert ``e``:
+  ``out[j, n] = sum_d x[perm[j] // k, d] * W[e, d, n]`` in float64 from the
+  bf16 inputs.
+
+Parity status: the pages print no worked example, so no function here is
+pinned to a value printed on the pages. Each is pinned instead by closed
+forms, invariants, library routines and brute force in
+``tests/test_oracle_pins.py``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle (gcc -O2) into a shared library next to its source."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        subprocess.check_call(["gcc", "-O2", "-std=c11", "-shared", "-fPIC", "-pthread",
+                               "-o", tmp, _SRC])
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+_lib = None
+_P = ctypes.c_void_p
+_I = ctypes.c_int64
+
+
+def _L():
+    global _lib
+    if _lib is None:
+        build()
+        lib = ctypes.CDLL(_LIB)
+        lib.oracle_bf16_to_f64.restype = ctypes.c_double
+        lib.oracle_bf16_to_f64.argtypes = [ctypes.c_uint16]
+        lib.oracle_route_counts.restype = ctypes.c_int
+        lib.oracle_route_counts.argtypes = [_P, _I, _I, _I, _P, _P]
+        lib.oracle_build_perm.restype = ctypes.c_int
+        lib.oracle_build_perm.argtypes = [_P, _I, _I, _I, _P, _P, _P]
+        lib.oracle_expert_of_row.restype = ctypes.c_int64
+        lib.oracle_expert_of_row.argtypes = [_P, _I, _I]
+        lib.oracle_gemm_rows.restype = ctypes.c_int
+        lib.oracle_gemm_rows.argtypes = [_P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _I, _P,
+                                         ctypes.c_int]
+        _lib = lib
+    return _lib
+
+
+class OracleError(ValueError):
+    pass
+
+
+def _c(a, dtype):
+    a = np.ascontiguousarray(a, dtype=dtype)
+    return a
+
+
+def route_counts(topk: np.ndarray, E: int):
+    """Return (counts int64[E], offsets int64[E+1])."""
+    topk = _c(topk, np.int32)
+    T, k = topk.shape
+    counts = np.zeros(E, dtype=np.int64)
+    offsets = np.zeros(E + 1, dtype=np.int64)
+    rc = _L().oracle_route_counts(topk.ctypes.data, T, k, E, counts.ctypes.data,
+                                  offsets.ctypes.data)
+    if rc:
+        raise OracleError("expert index outside [0, E)")
+    return counts, offsets
+
+
+def build_perm(topk: np.ndarray, E: int, offsets: np.ndarray):
+    """Return (perm int64[T*k], inv_perm int64[T*k])."""
+    topk = _c(topk, np.int32)
+    T, k = topk.shape
+    offsets = _c(offsets, np.int64)
+    perm = np.full(T * k, -1, dtype=np.int64)
+    inv = np.full(T * k, -1, dtype=np.int64)
+    rc = _L().oracle_build_perm(topk.ctypes.data, T, k, E, offsets.ctypes.data,
+                                perm.ctypes.data, inv.ctypes.data)
+    if rc:
+        raise OracleError("expert index outside [0, E)")
+    return perm, inv
+
+
+def expert_of_row(offsets: np.ndarray, j: int) -> int:
+    offsets = _c(offsets, np.int64)
+    return int(_L().oracle_expert_of_row(offsets.ctypes.data, offsets.size - 1, j))
+
+
+def gemm_rows(x: np.ndarray, perm: np.ndarray, offsets: np.ndarray, W: np.ndarray, k: int,
+              rows, threads: int | None = None) -> np.ndarray:
+    """float64 [len(rows), De]: the expert GEMM for the listed sorted rows."""
+    x = _c(x, np.uint16)
+    W = np.asarray(W)
+    assert W.dtype == np.uint16 and W.flags.c_contiguous
+    T, D = x.shape
+    E, D2, De = W.shape
+    assert D2 == D
+    perm = _c(perm, np.int64)
+    offsets = _c(offsets, np.int64)
+    rows = _c(np.asarray(rows).reshape(-1), np.int64)
+    out = np.zeros((rows.size, De), dtype=np.float64)
+    if rows.size:
+        rc = _L().oracle_gemm_rows(x.ctypes.data, perm.ctypes.data, offsets.ctypes.data,
+                                   W.ctypes.data, T, k, D, E, De, rows.ctypes.data, rows.size,
+                                   out.ctypes.data, threads or max(1, os.cpu_count() or 1))
+        if rc:
+            raise OracleError("row outside every expert segment, or token out of range")
+    return out
+
+
+def gemm_all(x, perm, offsets, W, k, threads=None) -> np.ndarray:
+    return gemm_rows(x, perm, offsets, W, k, np.arange(perm.size), threads)
+
+
+def bf16_to_f64(h: int) -> float:
+    return float(_L().oracle_bf16_to_f64(h))
+
+
+def run(topk, E, x=None, W=None, rows=None, threads=None):
+    """Whole path on the CPU: counts, offsets, perm, inv_perm and (if x, W
+    given) the GEMM for ``rows`` (all rows when None)."""
+    topk = np.asarray(topk)
+    counts, offsets = route_counts(topk, E)
+    perm, inv = build_perm(topk, E, offsets)
+    res = {"counts": counts, "offsets": offsets, "perm": perm, "inv_perm": inv}
+    if x is not None and W is not None:
+        k = topk.shape[1]
+        if rows is None:
+            rows = np.arange(perm.size)
+        res["rows"] = np.asarray(rows, dtype=np.int64)
+        res["out"] = gemm_rows(x, perm, offsets, W, k, rows, threads)
+    return res

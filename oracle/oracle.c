@@ -1,0 +1,145 @@
+/*
+ * ORACLE for MoE token dispatch + expert GEMM. TEST INFRASTRUCTURE ONLY.
+ *
+ * Only the tests, the smoke check and the benchmark's CPU-baseline leg may
+ * load this library. It shares no code with the CUDA path: no headers, no
+ * helpers, no tables. It is deliberately plain and slow: serial loops in the
+ * order the definitions are written, floating point in float64.
+ *
+ * What it computes (the expert-parallel "token-dispatch + GEMM" of
+ * "Loads and Loads of Fluffy Kittens", section "Key claims", Fig. 17, on one
+ * device): given routed expert indices topk[T][k],
+ *   1. count[e]   = number of (t, s) with topk[t][s] == e;
+ *   2. offsets[0] = 0, offsets[e+1] = offsets[e] + count[e];
+ *   3. perm       = the flat routing indices f = t*k + s listed expert by
+ *                   expert, and inside one expert by increasing f (token,
+ *                   then slot); inv_perm[f] = position of f in perm;
+ *   4. out[j][n]  = sum over d of x[perm[j] / k][d] * W[e(j)][d][n], where
+ *                   e(j) is the expert whose segment [offsets[e],
+ *                   offsets[e+1]) holds j. Inputs are bf16, the products
+ *                   and the sum are formed in float64, d ascending.
+ *
+ * All integer outputs are int64 so that nothing about their width is shared
+ * with the device path (which uses int32).
+ */
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* bf16 bit pattern -> float64; exact (bf16 is the top half of a float32). */
+double oracle_bf16_to_f64(uint16_t h) {
+    uint32_t u = (uint32_t)h << 16;
+    float f;
+    memcpy(&f, &u, 4);
+    return (double)f;
+}
+
+/* Step 1 and 2. Returns 0, or 1 if an index is outside [0, E). */
+int oracle_route_counts(const int32_t* topk, int64_t T, int64_t k, int64_t E,
+                        int64_t* counts, int64_t* offsets) {
+    for (int64_t e = 0; e < E; ++e) counts[e] = 0;
+    for (int64_t t = 0; t < T; ++t)
+        for (int64_t s = 0; s < k; ++s) {
+            int64_t e = topk[t * k + s];
+            if (e < 0 || e >= E) return 1;
+            counts[e] += 1;
+        }
+    offsets[0] = 0;
+    for (int64_t e = 0; e < E; ++e) offsets[e + 1] = offsets[e] + counts[e];
+    return 0;
+}
+
+/* Step 3: counting-sort scatter, visiting (t, s) in increasing order, so the
+ * order inside each expert's segment is the visiting order (stable). */
+int oracle_build_perm(const int32_t* topk, int64_t T, int64_t k, int64_t E,
+                      const int64_t* offsets, int64_t* perm, int64_t* inv_perm) {
+    int64_t* cursor = (int64_t*)malloc(sizeof(int64_t) * (size_t)(E > 0 ? E : 1));
+    if (!cursor) return 2;
+    for (int64_t e = 0; e < E; ++e) cursor[e] = offsets[e];
+    for (int64_t t = 0; t < T; ++t)
+        for (int64_t s = 0; s < k; ++s) {
+            int64_t f = t * k + s;
+            int64_t e = topk[f];
+            if (e < 0 || e >= E) { free(cursor); return 1; }
+            int64_t j = cursor[e]++;
+            perm[j] = f;
+            if (inv_perm) inv_perm[f] = j;
+        }
+    free(cursor);
+    return 0;
+}
+
+/* e(j): the expert whose segment holds row j (empty segments hold nothing). */
+int64_t oracle_expert_of_row(const int64_t* offsets, int64_t E, int64_t j) {
+    for (int64_t e = 0; e < E; ++e)
+        if (offsets[e] <= j && j < offsets[e + 1]) return e;
+    return -1;
+}
+
+/* Step 4 for one row j: out[n] for n in [0, De). */
+static int gemm_one_row(const uint16_t* x, const int64_t* perm, const int64_t* offsets,
+                        const uint16_t* W, int64_t T, int64_t k, int64_t D, int64_t E,
+                        int64_t De, int64_t j, double* out) {
+    int64_t e = oracle_expert_of_row(offsets, E, j);
+    if (e < 0) return 1;
+    int64_t t = perm[j] / k;
+    if (t < 0 || t >= T) return 1;
+    for (int64_t n = 0; n < De; ++n) out[n] = 0.0;
+    for (int64_t d = 0; d < D; ++d) {
+        double xv = oracle_bf16_to_f64(x[t * D + d]);
+        const uint16_t* wrow = W + ((size_t)e * (size_t)D + (size_t)d) * (size_t)De;
+        for (int64_t n = 0; n < De; ++n) out[n] += xv * oracle_bf16_to_f64(wrow[n]);
+    }
+    return 0;
+}
+
+typedef struct {
+    const uint16_t *x, *W;
+    const int64_t *perm, *offsets, *rows;
+    int64_t T, k, D, E, De, r0, r1;
+    double* out;
+    int status;
+} gemm_job;
+
+static void* gemm_worker(void* arg) {
+    gemm_job* g = (gemm_job*)arg;
+    g->status = 0;
+    for (int64_t r = g->r0; r < g->r1; ++r)
+        if (gemm_one_row(g->x, g->perm, g->offsets, g->W, g->T, g->k, g->D, g->E, g->De,
+                         g->rows[r], g->out + (size_t)r * (size_t)g->De))
+            g->status = 1;
+    return NULL;
+}
+
+/* Step 4 for the listed rows: out[r][n] = result for row rows[r].
+ * Threads split the list of rows; each row is computed by one thread in the
+ * serial order above, so the result does not depend on nthreads. */
+int oracle_gemm_rows(const uint16_t* x, const int64_t* perm, const int64_t* offsets,
+                     const uint16_t* W, int64_t T, int64_t k, int64_t D, int64_t E, int64_t De,
+                     const int64_t* rows, int64_t nrows, double* out, int nthreads) {
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > 256) nthreads = 256;
+    if (nthreads > nrows) nthreads = nrows > 0 ? (int)nrows : 1;
+    pthread_t th[256];
+    gemm_job jobs[256];
+    int created[256];
+    int64_t per = (nrows + nthreads - 1) / nthreads;
+    int n = 0;
+    for (int i = 0; i < nthreads; ++i) {
+        int64_t b = i * per, e = b + per;
+        if (b >= nrows) break;
+        if (e > nrows) e = nrows;
+        gemm_job g = {x, W, perm, offsets, rows, T, k, D, E, De, b, e, out, 0};
+        jobs[i] = g;
+        created[i] = (i < nthreads - 1) && pthread_create(&th[i], NULL, gemm_worker, &jobs[i]) == 0;
+        if (!created[i]) gemm_worker(&jobs[i]);
+        n = i + 1;
+    }
+    int status = 0;
+    for (int i = 0; i < n; ++i) {
+        if (created[i]) pthread_join(th[i], NULL);
+        status |= jobs[i].status;
+    }
+    return status;
+}

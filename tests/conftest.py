@@ -1,0 +1,25 @@
+import os
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+
+def pytest_configure(config):
+    config.addinivalue_line("markers", "gpu: needs a CUDA GPU (sm_103a) and the built CUDA library")
+    config.addinivalue_line("markers", "slow: full-size workload (seconds to minutes)")
+
+
+@pytest.fixture(scope="session")
+def gpu_lib():
+    """The CUDA library, built in-tree if missing; fails loudly without a GPU."""
+    import torch
+    if not torch.cuda.is_available():
+        pytest.fail("GPU test run without a CUDA device")
+    from moe_token_dispatch_gb300 import _build
+    _build.build()
+    import moe_token_dispatch_gb300 as pk
+    return pk

@@ -1,0 +1,277 @@
+"""Pins of the CPU oracle to facts outside itself (CPU only).
+
+The pages print no worked example for token dispatch, so the oracle is pinned
+by a hand-worked example, invariants of the routing, library routines
+(numpy bincount / stable argsort / float64 matmul), closed forms (identity and
+shifted-identity weights, all-ones weights) and brute force on tiny inputs.
+The last group plants mistakes in a small pure-Python copy of the path and
+checks that the same pins catch each of them.
+"""
+import math
+
+import numpy as np
+import pytest
+
+import inputgen as ig
+import oracle
+
+
+def bf16(v):
+    """float -> bf16 bits (values used here are exactly representable)."""
+    a = np.asarray(v, dtype=np.float32)
+    return (a.view(np.uint32) >> 16).astype(np.uint16)
+
+
+# ----------------------------------------------------------------- checkers
+def check_routing(topk, E, counts, offsets, perm, inv):
+    """All pins on counts / offsets / perm / inv_perm; raises AssertionError."""
+    T, k = topk.shape
+    R = T * k
+    flat = topk.reshape(-1)
+    # counts: library histogram
+    assert np.array_equal(counts, np.bincount(flat, minlength=E))
+    # offsets: exclusive prefix sum
+    assert offsets[0] == 0 and offsets[E] == R
+    assert np.array_equal(np.diff(offsets), counts)
+    # perm: a permutation of the flat indices
+    assert np.array_equal(np.sort(perm), np.arange(R))
+    # each token exactly k times
+    assert np.array_equal(np.bincount(perm // k, minlength=T), np.full(T, k))
+    # segment e holds only entries routed to e, in increasing flat order
+    for e in range(E):
+        seg = perm[offsets[e]:offsets[e + 1]]
+        assert np.all(flat[seg] == e)
+        assert np.all(np.diff(seg) > 0)
+    # the stable library sort of the expert ids gives the same order
+    assert np.array_equal(perm, np.argsort(flat, kind="stable"))
+    # inverse restores the routing
+    assert np.array_equal(inv[perm], np.arange(R))
+    assert np.array_equal(perm[inv], np.arange(R))
+    pos_expert = np.searchsorted(offsets, np.arange(R), side="right") - 1
+    assert np.array_equal(pos_expert[inv], flat)
+
+
+def check_gemm_closed_forms(path, rng):
+    """Pins on a GEMM function path(topk, E, x_bits, W_bits) -> (perm, offsets, out)."""
+    T, k, E, D, De = 9, 3, 5, 24, 16
+    topk = np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int32)
+    x = bf16(rng.integers(-64, 64, size=(T, D)) / 8.0)
+    # identity weights: row j reproduces x[perm[j] // k, :De] exactly
+    W = np.zeros((E, D, De), dtype=np.float32)
+    for e in range(E):
+        W[e, :De, :De] = np.eye(De)
+    perm, offsets, out = path(topk, E, x, bf16(W))
+    xf = ig.bf16_bits_to_f64(x)
+    assert np.array_equal(out, xf[perm // k][:, :De])
+    # shifted identity W[e, d, n] = [d == (n + e) mod D]: proves which expert is used
+    W = np.zeros((E, D, De), dtype=np.float32)
+    for e in range(E):
+        for n in range(De):
+            W[e, (n + e) % D, n] = 1.0
+    perm, offsets, out = path(topk, E, x, bf16(W))
+    ex = np.searchsorted(offsets, np.arange(T * k), side="right") - 1
+    cols = (np.arange(De)[None, :] + ex[:, None]) % D
+    assert np.array_equal(out, xf[(perm // k)[:, None], cols])
+    # all-ones weights: every column is the exact row sum (math.fsum)
+    W = np.ones((E, D, De), dtype=np.float32)
+    perm, offsets, out = path(topk, E, x, bf16(W))
+    for j in range(T * k):
+        s = math.fsum(xf[perm[j] // k])
+        assert np.all(out[j] == s)
+
+
+def check_gemm_library(path, rng, T=40, k=2, E=6, D=96, De=40):
+    """float64 matmul of the gathered rows, expert by expert, and brute force."""
+    logits = rng.standard_normal((T, E))
+    topk = np.argsort(-logits, axis=1, kind="stable")[:, :k].astype(np.int32)
+    x = bf16(rng.standard_normal((T, D)).astype(np.float32))
+    W = bf16((rng.standard_normal((E, D, De)) / np.sqrt(D)).astype(np.float32))
+    perm, offsets, out = path(topk, E, x, W)
+    xf, wf = ig.bf16_bits_to_f64(x), ig.bf16_bits_to_f64(W)
+    for e in range(E):
+        lo, hi = offsets[e], offsets[e + 1]
+        ref = xf[perm[lo:hi] // k] @ wf[e]
+        scale = np.abs(xf[perm[lo:hi] // k]) @ np.abs(wf[e]) + 1e-300
+        assert np.all(np.abs(out[lo:hi] - ref) <= 1e-12 * scale)
+    # brute force with exact summation on a few rows
+    for j in (0, T * k // 2, T * k - 1):
+        e = int(np.searchsorted(offsets, j, side="right") - 1)
+        t = perm[j] // k
+        for n in (0, De // 3, De - 1):
+            exact = math.fsum(xf[t, d] * wf[e, d, n] for d in range(D))
+            assert abs(out[j, n] - exact) <= 1e-12 * sum(abs(xf[t, d] * wf[e, d, n]) for d in range(D))
+
+
+def oracle_path(topk, E, x, W):
+    res = oracle.run(topk, E, x, W)
+    return res["perm"], res["offsets"], res["out"]
+
+
+# ------------------------------------------------------------ oracle pins
+def test_hand_worked_example():
+    # T=4 tokens, k=2 slots, E=4 experts (expert 3 receives nothing).
+    # flat index f = t*k + s:  f: 0 1 2 3 4 5 6 7
+    #                   expert: 2 0 0 2 1 2 2 1
+    topk = np.array([[2, 0], [0, 2], [1, 2], [2, 1]], dtype=np.int32)
+    counts, offsets = oracle.route_counts(topk, 4)
+    assert counts.tolist() == [2, 2, 4, 0]
+    assert offsets.tolist() == [0, 2, 4, 8, 8]
+    perm, inv = oracle.build_perm(topk, 4, offsets)
+    # expert 0: f=1,2; expert 1: f=4,7; expert 2: f=0,3,5,6
+    assert perm.tolist() == [1, 2, 4, 7, 0, 3, 5, 6]
+    assert inv.tolist() == [4, 0, 1, 5, 2, 6, 7, 3]
+    # GEMM with D=2, De=2 and small exact weights, worked by hand:
+    x = bf16([[1, 2], [3, -1], [0.5, 4], [-2, 1]])
+    W = bf16([[[1, 0], [0, 1]], [[2, 1], [0, 1]], [[1, 1], [1, -1]], [[0, 0], [0, 0]]])
+    out = oracle.gemm_all(x, perm, offsets, W, 2)
+    expect = [[1, 2], [3, -1],            # expert 0 (identity): tokens 0, 1
+              [1, 4.5], [-4, -1],          # expert 1: tokens 2, 3
+              [3, -1], [2, 4], [4.5, -3.5], [-1, -3]]  # expert 2: tokens 0, 1, 2, 3
+    assert out.tolist() == expect
+    assert oracle.expert_of_row(offsets, 3) == 1 and oracle.expert_of_row(offsets, 8) == -1
+
+
+@pytest.mark.parametrize("name", ["tiny", "mid"])
+def test_routing_invariants_on_workloads(name):
+    wl = ig.WORKLOADS[name]
+    topk = ig.make_topk(wl)
+    counts, offsets = oracle.route_counts(topk, wl.E)
+    perm, inv = oracle.build_perm(topk, wl.E, offsets)
+    check_routing(topk, wl.E, counts, offsets, perm, inv)
+
+
+def test_routing_invariants_with_duplicates_and_empty_experts():
+    rng = np.random.default_rng(3)
+    for T, k, E in [(1, 1, 1), (7, 3, 2), (50, 4, 9), (300, 2, 40)]:
+        topk = rng.integers(0, max(1, E // 2), size=(T, k)).astype(np.int32)  # upper experts empty
+        counts, offsets = oracle.route_counts(topk, E)
+        perm, inv = oracle.build_perm(topk, E, offsets)
+        check_routing(topk, E, counts, offsets, perm, inv)
+    # brute-force counts and the (expert, token, slot) order with sorted()
+    topk = rng.integers(0, 5, size=(11, 3)).astype(np.int32)
+    counts, offsets = oracle.route_counts(topk, 5)
+    assert counts.tolist() == [sum(1 for t in range(11) for s in range(3) if topk[t, s] == e)
+                               for e in range(5)]
+    perm, _ = oracle.build_perm(topk, 5, offsets)
+    order = sorted(((int(topk[t, s]), t, s) for t in range(11) for s in range(3)))
+    assert perm.tolist() == [t * 3 + s for _, t, s in order]
+
+
+def test_bad_index_is_rejected():
+    with pytest.raises(oracle.OracleError):
+        oracle.route_counts(np.array([[0, 4]], dtype=np.int32), 4)
+    with pytest.raises(oracle.OracleError):
+        oracle.route_counts(np.array([[-1, 0]], dtype=np.int32), 4)
+
+
+def test_empty_input():
+    topk = np.zeros((0, 3), dtype=np.int32)
+    counts, offsets = oracle.route_counts(topk, 5)
+    assert counts.tolist() == [0] * 5 and offsets.tolist() == [0] * 6
+    perm, inv = oracle.build_perm(topk, 5, offsets)
+    assert perm.size == 0 and inv.size == 0
+
+
+def test_gemm_closed_forms():
+    check_gemm_closed_forms(oracle_path, np.random.default_rng(5))
+
+
+def test_gemm_against_float64_matmul_and_brute_force():
+    check_gemm_library(oracle_path, np.random.default_rng(6))
+
+
+def test_gemm_tiny_workload_against_matmul():
+    wl = ig.WORKLOADS["tiny"]
+    case = ig.make_case(wl)
+    res = oracle.run(case.topk, wl.E, case.x, case.W)
+    xf, wf = ig.bf16_bits_to_f64(case.x), ig.bf16_bits_to_f64(case.W)
+    off, perm = res["offsets"], res["perm"]
+    for e in range(wl.E):
+        rows = perm[off[e]:off[e + 1]] // wl.k
+        ref = xf[rows] @ wf[e]
+        scale = np.abs(xf[rows]) @ np.abs(wf[e])
+        assert np.all(np.abs(res["out"][off[e]:off[e + 1]] - ref) <= 1e-12 * scale)
+
+
+def test_gemm_rows_independent_of_threads_and_subset():
+    wl = ig.custom(T=33, D=64, E=4, k=2, De=24)
+    case = ig.make_case(wl)
+    full = oracle.run(case.topk, wl.E, case.x, case.W, threads=1)
+    rows = np.array([65, 0, 17, 17, 3])
+    part = oracle.gemm_rows(case.x, full["perm"], full["offsets"], case.W, wl.k, rows, threads=3)
+    assert np.array_equal(part, full["out"][rows])
+
+
+# ------------------------------------------- planted mistakes are caught
+def python_path(topk, E, x, W, bug=None):
+    """A small pure-Python copy of the path, used only to plant mistakes."""
+    T, k = topk.shape
+    flat = topk.reshape(-1)
+    counts = np.zeros(E, dtype=np.int64)
+    for e in flat:
+        counts[e] += 1
+    offsets = np.zeros(E + 1, dtype=np.int64)
+    offsets[1:] = np.cumsum(counts)
+    if bug == "inclusive_scan":
+        offsets[:-1] = offsets[1:]
+    if bug == "slot_major":     # (expert, slot, token) instead of (expert, token, slot)
+        order = sorted(range(T * k), key=lambda f: (flat[f], f % k, f // k))
+    else:
+        order = sorted(range(T * k), key=lambda f: (flat[f], f))
+    perm = np.array(order, dtype=np.int64)
+    xf, wf = ig.bf16_bits_to_f64(x), ig.bf16_bits_to_f64(W)
+    De = W.shape[2]
+    out = np.zeros((T * k, De))
+    for j in range(T * k):
+        e = int(np.searchsorted(offsets, j, side="right") - 1)
+        t = perm[j] // k
+        if bug == "token_mod":
+            t = perm[j] % k
+        if bug == "expert_minus_one":
+            e = max(e - 1, 0)
+        w = wf[e]
+        if bug == "reversed_k":   # W read along d in the wrong direction
+            w = wf[e][::-1]
+        D = xf.shape[1]
+        dmax = D - 1 if bug == "dropped_term" else D
+        out[j] = xf[t, :dmax] @ w[:dmax]
+    inv = np.empty_like(perm)
+    inv[perm] = np.arange(T * k)
+    return counts, offsets, perm, inv, out
+
+
+def test_python_copy_passes_all_pins():
+    rng = np.random.default_rng(8)
+    topk = np.stack([rng.permutation(6)[:3] for _ in range(20)]).astype(np.int32)
+    counts, offsets, perm, inv, _ = python_path(topk, 6, np.zeros((20, 1), np.uint16),
+                                                np.zeros((6, 1, 1), np.uint16))
+    check_routing(topk, 6, counts, offsets, perm, inv)
+    def p(tk, E, x, W):
+        _, offsets, perm, _, out = python_path(tk, E, x, W)
+        return perm, offsets, out
+    check_gemm_closed_forms(p, np.random.default_rng(5))
+    check_gemm_library(p, np.random.default_rng(6))
+
+
+@pytest.mark.parametrize("bug", ["inclusive_scan", "slot_major"])
+def test_planted_routing_mistakes_are_caught(bug):
+    rng = np.random.default_rng(9)
+    topk = np.stack([rng.permutation(6)[:3] for _ in range(20)]).astype(np.int32)
+    counts, offsets, perm, inv, _ = python_path(topk, 6, np.zeros((20, 1), np.uint16),
+                                                np.zeros((6, 1, 1), np.uint16), bug)
+    with pytest.raises(AssertionError):
+        check_routing(topk, 6, counts, offsets, perm, inv)
+
+
+@pytest.mark.parametrize("bug", ["token_mod", "expert_minus_one", "reversed_k", "dropped_term"])
+def test_planted_gemm_mistakes_are_caught(bug):
+    def p(tk, E, x, W):
+        _, offsets, perm, _, out = python_path(tk, E, x, W, bug)
+        return perm, offsets, out
+    caught = 0
+    for checker, seed in ((check_gemm_closed_forms, 5), (check_gemm_library, 6)):
+        try:
+            checker(p, np.random.default_rng(seed))
+        except AssertionError:
+            caught += 1
+    assert caught >= 1
