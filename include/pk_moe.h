@@ -1,0 +1,153 @@
+/*
+ * pk_moe.h -- C ABI of the GB300 (sm_103a) MoE token-dispatch + expert-GEMM
+ * library, libpkmoe.so.
+ *
+ * The operation is the single-device core of the expert-parallel
+ * "token-dispatch + GEMM" of "Loads and Loads of Fluffy Kittens" (section
+ * "Key claims", Fig. 17: top_k=8, num_experts=256, D=7168, D_expert=2048;
+ * "Results", last item): tokens routed to experts are grouped expert by
+ * expert, and each group is multiplied by its expert's up-projection weight.
+ *
+ * Tensors (all row-major, all in DEVICE memory, all owned and allocated by the
+ * caller; the library allocates no device memory in any call):
+ *   x              bf16  [T, D]            token activations
+ *   topk_idx       int32 [T, k]            routed experts; slot s of token t
+ *   W              bf16  [E, D, D_expert]  expert up-projection weights
+ *   expert_counts  int32 [E]               rows routed to each expert
+ *   expert_offsets int32 [E + 1]           exclusive prefix sum of the counts
+ *   perm           int32 [T*k]             sorted row j -> flat index t*k+s
+ *   inv_perm       int32 [T*k]             flat index t*k+s -> sorted row j
+ *   out            bf16  [T*k, D_expert]   row j = x[perm[j] / k] @ W[e(j)]
+ * bf16 tensors are passed as uint16_t bit patterns.
+ *
+ * Calls are asynchronous on `stream` (a cudaStream_t passed as void*; NULL is
+ * the legacy default stream) and do not synchronise. route_counts ->
+ * build_perm -> dispatch_gemm must be ordered on one stream (or by events).
+ * Calls on distinct streams with distinct buffers are thread safe.
+ *
+ * Return value: PK_OK, or the first synchronous failure -- argument checks
+ * (PK_ERR_INVALID_ARG, PK_ERR_UNSUPPORTED) or a failed launch (PK_ERR_CUDA).
+ * Errors found on the device are written to *status_word (int32, device
+ * memory, nullable): the first error code sticks until the caller clears it.
+ * PK_ERR_BAD_INDEX means an expert index outside [0, E) (that entry is left
+ * out of counts and perm, so outputs are incomplete); PK_ERR_TIMEOUT means a
+ * bounded pipeline wait inside the GEMM ran out (outputs incomplete, the
+ * kernel returned normally and the context stays usable).
+ */
+#ifndef PK_MOE_H
+#define PK_MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    PK_OK = 0,
+    PK_ERR_INVALID_ARG = 1,
+    PK_ERR_UNSUPPORTED = 2,
+    PK_ERR_CUDA = 3,
+    PK_ERR_TIMEOUT = 4,
+    PK_ERR_BAD_INDEX = 5
+} pk_status;
+
+/* Largest number of experts the routing kernels accept. */
+#define PK_MAX_EXPERTS 4096
+
+/* Static string naming a status code (never NULL). */
+const char* pk_status_str(int status);
+
+/* Version of this ABI (major * 10000 + minor * 100 + patch). */
+int pk_abi_version(void);
+
+/*
+ * Bytes of device workspace that pk_moe_route_counts and pk_moe_build_perm
+ * need for (T, k, E): per-block expert histograms that become per-block
+ * starting positions. 0 when T*k == 0. Pure host arithmetic.
+ */
+size_t pk_moe_workspace_bytes(int32_t T, int32_t k, int32_t E);
+
+/*
+ * Routing histogram and exclusive scan ("route tokens to experts", the
+ * dispatch half of the token-dispatch + GEMM result, "Key claims", Fig. 17):
+ *   expert_counts[e]    = #{(t, s) : topk_idx[t, s] == e}
+ *   expert_offsets[0]   = 0,  expert_offsets[e+1] = expert_offsets[e] + expert_counts[e]
+ * so expert_offsets[E] == T*k when every index is in range.
+ *   topk_idx        device int32 [T, k], read only
+ *   expert_counts   device int32 [E], written; may be NULL
+ *   expert_offsets  device int32 [E + 1], written
+ *   workspace       device, >= pk_moe_workspace_bytes(T, k, E) bytes, 16-byte
+ *                   aligned; written here and read by pk_moe_build_perm
+ *   status_word     device int32, nullable (see above)
+ * Requires T >= 0, 1 <= k <= E <= PK_MAX_EXPERTS, T*k < 2^31. T == 0 writes
+ * zero offsets.
+ */
+int pk_moe_route_counts(const int32_t* topk_idx, int32_t T, int32_t k, int32_t E,
+                        int32_t* expert_counts, int32_t* expert_offsets,
+                        void* workspace, size_t workspace_bytes,
+                        int32_t* status_word, void* stream);
+
+/*
+ * Stable permutation of the routed rows, ordered by expert, then token, then
+ * slot: for every flat index f = t*k + s with e = topk_idx[t, s],
+ *   perm[expert_offsets[e] + r] = f,   inv_perm[f] = expert_offsets[e] + r,
+ * where r = #{f' < f : topk_idx.flat[f'] == e}.
+ *   topk_idx, expert_offsets  device int32, read only (offsets from
+ *                   pk_moe_route_counts on the same topk_idx)
+ *   perm            device int32 [T*k], written
+ *   inv_perm        device int32 [T*k], written; may be NULL
+ *   workspace       the workspace that pk_moe_route_counts filled for the same
+ *                   topk_idx, T, k, E, unmodified since
+ * Positions outside [0, T*k) (a workspace that does not match) are never
+ * written; they set PK_ERR_BAD_INDEX.
+ */
+int pk_moe_build_perm(const int32_t* topk_idx, int32_t T, int32_t k, int32_t E,
+                      const int32_t* expert_offsets, int32_t* perm, int32_t* inv_perm,
+                      const void* workspace, size_t workspace_bytes,
+                      int32_t* status_word, void* stream);
+
+/*
+ * Token dispatch fused with the expert GEMM ("token-dispatch + GEMM", "Key
+ * claims", Fig. 17): for every expert e and sorted row j in
+ * [expert_offsets[e], expert_offsets[e+1]),
+ *   out[j, n] = bf16_rne( sum_d x[perm[j] / k, d] * W[e, d, n] )
+ * with bf16 products accumulated in fp32 on the tensor cores. The gathered
+ * rows are never written to memory: they are gathered from x straight into
+ * shared memory. Experts with no rows cost nothing and their W is not read.
+ *   x        device bf16 [T, D], 16-byte aligned
+ *   perm     device int32 [T*k]; expert_offsets device int32 [E + 1]
+ *   W        device bf16 [E, D, D_expert], 16-byte aligned
+ *   out      device bf16 [T*k, D_expert], 16-byte aligned; rows of each expert
+ *            segment written, nothing else
+ * Requires T >= 0, k >= 1, E >= 1, D >= 1, D_expert >= 1, D and D_expert
+ * multiples of 8, T*k < 2^31. Offsets are clamped into [0, T*k] and perm
+ * entries into range, so no input makes the kernel touch memory outside the
+ * buffers above; a perm entry outside [0, T*k) sets PK_ERR_BAD_INDEX.
+ */
+int pk_moe_dispatch_gemm(const uint16_t* x, const int32_t* perm, const int32_t* expert_offsets,
+                         const uint16_t* W, int32_t T, int32_t k, int32_t D, int32_t E,
+                         int32_t D_expert, uint16_t* out, int32_t* status_word, void* stream);
+
+/*
+ * Limit, in nanoseconds, on every pipeline wait inside the GEMM kernel
+ * (default 4e9). A wait that runs out sets PK_ERR_TIMEOUT and the kernel
+ * drains its own copies and returns. Applies to later launches from this
+ * process. 0 restores the default.
+ */
+void pk_moe_set_wait_limit_ns(uint64_t limit_ns);
+
+/*
+ * Failure-detection check of the bounded wait used by the GEMM pipeline: one
+ * block waits on a shared-memory barrier that nothing ever completes, gives
+ * up after `limit_ns` and writes PK_ERR_TIMEOUT to *status_word (device
+ * int32). Returns PK_OK if the launch succeeded.
+ */
+int pk_debug_bounded_wait(int32_t* status_word, uint64_t limit_ns, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PK_MOE_H */

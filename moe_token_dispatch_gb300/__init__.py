@@ -1,0 +1,30 @@
+"""GB300 (sm_103a) MoE token dispatch + expert GEMM.
+
+The hot path -- routing histogram and scan, stable (expert, token, slot)
+permutation, and the per-expert GEMM fed by a row gather -- runs in the CUDA
+kernels of ``libpkmoe.so`` behind the C ABI in ``include/pk_moe.h``. This
+package is its ctypes binding (same function names) plus ``MoeDispatch``, a
+holder of the device buffers one step needs. PyTorch provides device memory
+and streams only.
+"""
+from ._binding import (  # noqa: F401
+    LIB_PATH,
+    PK_ERR_BAD_INDEX,
+    PK_ERR_CUDA,
+    PK_ERR_INVALID_ARG,
+    PK_ERR_TIMEOUT,
+    PK_ERR_UNSUPPORTED,
+    PK_MAX_EXPERTS,
+    PK_OK,
+    PkError,
+    lib,
+    pk_abi_version,
+    pk_debug_bounded_wait,
+    pk_moe_build_perm,
+    pk_moe_dispatch_gemm,
+    pk_moe_route_counts,
+    pk_moe_set_wait_limit_ns,
+    pk_moe_workspace_bytes,
+    pk_status_str,
+)
+from .dispatch import MoeDispatch  # noqa: F401

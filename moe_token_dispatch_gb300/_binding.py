@@ -1,0 +1,160 @@
+"""ctypes binding of libpkmoe.so: argument marshalling only.
+
+Each function has the name of the C entry point it calls and takes torch
+tensors that must already live on the GPU with the dtype and layout the C ABI
+documents (``include/pk_moe.h``). Nothing here computes any part of the path;
+if the library is missing the import fails loudly.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libpkmoe.so")
+
+PK_OK = 0
+PK_ERR_INVALID_ARG = 1
+PK_ERR_UNSUPPORTED = 2
+PK_ERR_CUDA = 3
+PK_ERR_TIMEOUT = 4
+PK_ERR_BAD_INDEX = 5
+PK_MAX_EXPERTS = 4096
+
+
+class PkError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {pk_status_str(code)} ({code})")
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"{LIB_PATH} is not built: run moe_token_dispatch_gb300._build.build() "
+                          "(or __graft_entry__.build()) first")
+    lib = ctypes.CDLL(LIB_PATH)
+    P, I32, SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t
+    lib.pk_status_str.restype = ctypes.c_char_p
+    lib.pk_status_str.argtypes = [ctypes.c_int]
+    lib.pk_abi_version.restype = ctypes.c_int
+    lib.pk_abi_version.argtypes = []
+    lib.pk_moe_workspace_bytes.restype = SZ
+    lib.pk_moe_workspace_bytes.argtypes = [I32, I32, I32]
+    lib.pk_moe_route_counts.restype = ctypes.c_int
+    lib.pk_moe_route_counts.argtypes = [P, I32, I32, I32, P, P, P, SZ, P, P]
+    lib.pk_moe_build_perm.restype = ctypes.c_int
+    lib.pk_moe_build_perm.argtypes = [P, I32, I32, I32, P, P, P, P, SZ, P, P]
+    lib.pk_moe_dispatch_gemm.restype = ctypes.c_int
+    lib.pk_moe_dispatch_gemm.argtypes = [P, P, P, P, I32, I32, I32, I32, I32, P, P, P]
+    lib.pk_moe_set_wait_limit_ns.restype = None
+    lib.pk_moe_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
+    lib.pk_debug_bounded_wait.restype = ctypes.c_int
+    lib.pk_debug_bounded_wait.argtypes = [P, ctypes.c_uint64, P]
+    return lib
+
+
+lib = _load()
+
+
+# ----------------------------------------------------------------- helpers
+def _ptr(t: torch.Tensor | None, dtype, name: str, numel: int | None = None):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name}: expected a torch.Tensor")
+    if t.device.type != "cuda":
+        raise ValueError(f"{name}: must be a CUDA tensor (got {t.device})")
+    if t.dtype != dtype:
+        raise TypeError(f"{name}: expected {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: must be contiguous")
+    if numel is not None and t.numel() < numel:
+        raise ValueError(f"{name}: needs at least {numel} elements, has {t.numel()}")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    if isinstance(stream, torch.cuda.Stream):
+        stream = stream.cuda_stream
+    return ctypes.c_void_p(int(stream))
+
+
+def _check(rc: int, where: str):
+    if rc != PK_OK:
+        raise PkError(rc, where)
+
+
+# ------------------------------------------------------- the C entry points
+def pk_status_str(code: int) -> str:
+    return lib.pk_status_str(int(code)).decode()
+
+
+def pk_abi_version() -> int:
+    return int(lib.pk_abi_version())
+
+
+def pk_moe_workspace_bytes(T: int, k: int, E: int) -> int:
+    return int(lib.pk_moe_workspace_bytes(T, k, E))
+
+
+def pk_moe_route_counts(topk_idx: torch.Tensor, E: int, expert_offsets: torch.Tensor,
+                        expert_counts: torch.Tensor | None = None,
+                        workspace: torch.Tensor | None = None,
+                        status_word: torch.Tensor | None = None, stream=None) -> None:
+    T, k = topk_idx.shape
+    ws_bytes = pk_moe_workspace_bytes(T, k, E)
+    if workspace is None:
+        raise ValueError("workspace: pass a uint8 CUDA tensor of pk_moe_workspace_bytes(T, k, E) bytes")
+    rc = lib.pk_moe_route_counts(
+        _ptr(topk_idx, torch.int32, "topk_idx"), T, k, E,
+        _ptr(expert_counts, torch.int32, "expert_counts", E),
+        _ptr(expert_offsets, torch.int32, "expert_offsets", E + 1),
+        _ptr(workspace, torch.uint8, "workspace", ws_bytes), workspace.numel(),
+        _ptr(status_word, torch.int32, "status_word", 1), _stream(stream))
+    _check(rc, "pk_moe_route_counts")
+
+
+def pk_moe_build_perm(topk_idx: torch.Tensor, E: int, expert_offsets: torch.Tensor,
+                      perm: torch.Tensor, inv_perm: torch.Tensor | None = None,
+                      workspace: torch.Tensor | None = None,
+                      status_word: torch.Tensor | None = None, stream=None) -> None:
+    T, k = topk_idx.shape
+    if workspace is None:
+        raise ValueError("workspace: pass the workspace filled by pk_moe_route_counts")
+    rc = lib.pk_moe_build_perm(
+        _ptr(topk_idx, torch.int32, "topk_idx"), T, k, E,
+        _ptr(expert_offsets, torch.int32, "expert_offsets", E + 1),
+        _ptr(perm, torch.int32, "perm", T * k),
+        _ptr(inv_perm, torch.int32, "inv_perm", T * k),
+        _ptr(workspace, torch.uint8, "workspace"), workspace.numel(),
+        _ptr(status_word, torch.int32, "status_word", 1), _stream(stream))
+    _check(rc, "pk_moe_build_perm")
+
+
+def pk_moe_dispatch_gemm(x: torch.Tensor, perm: torch.Tensor, expert_offsets: torch.Tensor,
+                         W: torch.Tensor, k: int, out: torch.Tensor,
+                         status_word: torch.Tensor | None = None, stream=None) -> None:
+    T, D = x.shape
+    E, D2, De = W.shape
+    if D2 != D:
+        raise ValueError(f"W is [E, {D2}, De] but x has D={D}")
+    rc = lib.pk_moe_dispatch_gemm(
+        _ptr(x, torch.bfloat16, "x"), _ptr(perm, torch.int32, "perm", T * k),
+        _ptr(expert_offsets, torch.int32, "expert_offsets", E + 1),
+        _ptr(W, torch.bfloat16, "W"), T, k, D, E, De,
+        _ptr(out, torch.bfloat16, "out", T * k * De),
+        _ptr(status_word, torch.int32, "status_word", 1), _stream(stream))
+    _check(rc, "pk_moe_dispatch_gemm")
+
+
+def pk_moe_set_wait_limit_ns(limit_ns: int) -> None:
+    lib.pk_moe_set_wait_limit_ns(int(limit_ns))
+
+
+def pk_debug_bounded_wait(status_word: torch.Tensor, limit_ns: int, stream=None) -> None:
+    rc = lib.pk_debug_bounded_wait(_ptr(status_word, torch.int32, "status_word", 1), int(limit_ns),
+                                   _stream(stream))
+    _check(rc, "pk_debug_bounded_wait")

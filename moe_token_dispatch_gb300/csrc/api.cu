@@ -1,0 +1,103 @@
+// extern "C" entry points of libpkmoe.so: argument checks, then launches.
+// Every check that can fail runs before any CUDA call, so a rejected call
+// touches neither the device nor the stream.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <atomic>
+
+#include "pk_internal.h"
+
+namespace {
+
+constexpr uint64_t kDefaultWaitLimitNs = 4000000000ull;
+std::atomic<uint64_t> g_wait_limit_ns{kDefaultWaitLimitNs};
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
+extern "C" {
+
+const char* pk_status_str(int status) {
+    switch (status) {
+        case PK_OK: return "PK_OK";
+        case PK_ERR_INVALID_ARG: return "PK_ERR_INVALID_ARG";
+        case PK_ERR_UNSUPPORTED: return "PK_ERR_UNSUPPORTED";
+        case PK_ERR_CUDA: return "PK_ERR_CUDA";
+        case PK_ERR_TIMEOUT: return "PK_ERR_TIMEOUT";
+        case PK_ERR_BAD_INDEX: return "PK_ERR_BAD_INDEX";
+        default: return "PK_ERR_UNKNOWN";
+    }
+}
+
+int pk_abi_version(void) { return 10000; }
+
+size_t pk_moe_workspace_bytes(int32_t T, int32_t k, int32_t E) {
+    if (T <= 0 || k <= 0 || E <= 0) return 0;
+    const int64_t R = static_cast<int64_t>(T) * k;
+    const size_t bytes = static_cast<size_t>(pk::route_blocks(R)) * static_cast<size_t>(E) * 4u;
+    return (bytes + 255u) & ~static_cast<size_t>(255u);
+}
+
+int pk_moe_route_counts(const int32_t* topk_idx, int32_t T, int32_t k, int32_t E,
+                        int32_t* expert_counts, int32_t* expert_offsets, void* workspace,
+                        size_t workspace_bytes, int32_t* status_word, void* stream) {
+    if (T < 0 || k < 1 || E < 1 || k > E || !expert_offsets) return PK_ERR_INVALID_ARG;
+    if (E > PK_MAX_EXPERTS) return PK_ERR_UNSUPPORTED;
+    const int64_t R = static_cast<int64_t>(T) * k;
+    if (R >= (int64_t{1} << 31)) return PK_ERR_UNSUPPORTED;
+    if (R > 0 && (!topk_idx || !workspace)) return PK_ERR_INVALID_ARG;
+    if (workspace_bytes < pk_moe_workspace_bytes(T, k, E)) return PK_ERR_INVALID_ARG;
+    if (workspace && !aligned16(workspace)) return PK_ERR_INVALID_ARG;
+    cudaError_t err = pk::launch_route_counts(topk_idx, static_cast<int32_t>(R), E, expert_counts,
+                                              expert_offsets, static_cast<int32_t*>(workspace),
+                                              status_word, static_cast<cudaStream_t>(stream));
+    return err == cudaSuccess ? PK_OK : PK_ERR_CUDA;
+}
+
+int pk_moe_build_perm(const int32_t* topk_idx, int32_t T, int32_t k, int32_t E,
+                      const int32_t* expert_offsets, int32_t* perm, int32_t* inv_perm,
+                      const void* workspace, size_t workspace_bytes, int32_t* status_word,
+                      void* stream) {
+    if (T < 0 || k < 1 || E < 1 || k > E) return PK_ERR_INVALID_ARG;
+    if (E > PK_MAX_EXPERTS) return PK_ERR_UNSUPPORTED;
+    const int64_t R = static_cast<int64_t>(T) * k;
+    if (R >= (int64_t{1} << 31)) return PK_ERR_UNSUPPORTED;
+    if (R == 0) return PK_OK;
+    if (!topk_idx || !expert_offsets || !perm || !workspace) return PK_ERR_INVALID_ARG;
+    if (workspace_bytes < pk_moe_workspace_bytes(T, k, E) || !aligned16(workspace))
+        return PK_ERR_INVALID_ARG;
+    cudaError_t err = pk::launch_build_perm(topk_idx, static_cast<int32_t>(R), E,
+                                            static_cast<const int32_t*>(workspace), perm, inv_perm,
+                                            status_word, static_cast<cudaStream_t>(stream));
+    return err == cudaSuccess ? PK_OK : PK_ERR_CUDA;
+}
+
+int pk_moe_dispatch_gemm(const uint16_t* x, const int32_t* perm, const int32_t* expert_offsets,
+                         const uint16_t* W, int32_t T, int32_t k, int32_t D, int32_t E,
+                         int32_t D_expert, uint16_t* out, int32_t* status_word, void* stream) {
+    if (T < 0 || k < 1 || E < 1 || D < 1 || D_expert < 1) return PK_ERR_INVALID_ARG;
+    if ((D % 8) != 0 || (D_expert % 8) != 0) return PK_ERR_INVALID_ARG;
+    const int64_t R = static_cast<int64_t>(T) * k;
+    if (R >= (int64_t{1} << 31)) return PK_ERR_UNSUPPORTED;
+    if (R == 0) return PK_OK;
+    if (!x || !perm || !expert_offsets || !W || !out) return PK_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(W) || !aligned16(out)) return PK_ERR_INVALID_ARG;
+    return pk::launch_dispatch_gemm(x, perm, expert_offsets, W, T, k, D, E, D_expert, out,
+                                    status_word, static_cast<cudaStream_t>(stream),
+                                    g_wait_limit_ns.load(std::memory_order_relaxed));
+}
+
+void pk_moe_set_wait_limit_ns(uint64_t limit_ns) {
+    g_wait_limit_ns.store(limit_ns ? limit_ns : kDefaultWaitLimitNs, std::memory_order_relaxed);
+}
+
+int pk_debug_bounded_wait(int32_t* status_word, uint64_t limit_ns, void* stream) {
+    if (!status_word || limit_ns == 0) return PK_ERR_INVALID_ARG;
+    cudaError_t err =
+        pk::launch_bounded_wait_probe(status_word, limit_ns, static_cast<cudaStream_t>(stream));
+    return err == cudaSuccess ? PK_OK : PK_ERR_CUDA;
+}
+
+}  // extern "C"

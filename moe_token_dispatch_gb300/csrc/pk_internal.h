@@ -1,0 +1,33 @@
+// Host-side declarations shared by the translation units of libpkmoe.so.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "pk_moe.h"
+
+namespace pk {
+
+// Routing: entries of topk_idx (flattened, t*k + s) handled by one block.
+constexpr int kRouteChunk = 2048;
+constexpr int kRouteThreads = 256;
+constexpr int kRouteWarps = kRouteThreads / 32;
+
+inline int route_blocks(int64_t R) { return static_cast<int>((R + kRouteChunk - 1) / kRouteChunk); }
+
+cudaError_t launch_route_counts(const int32_t* topk, int32_t R, int32_t E, int32_t* counts,
+                                int32_t* offsets, int32_t* blockbase, int32_t* status,
+                                cudaStream_t stream);
+cudaError_t launch_build_perm(const int32_t* topk, int32_t R, int32_t E,
+                              const int32_t* blockbase, int32_t* perm, int32_t* inv_perm,
+                              int32_t* status, cudaStream_t stream);
+
+// Dispatch GEMM. Returns PK_OK or a pk_status for host-side failures.
+int launch_dispatch_gemm(const uint16_t* x, const int32_t* perm, const int32_t* offsets,
+                         const uint16_t* W, int32_t T, int32_t k, int32_t D, int32_t E,
+                         int32_t De, uint16_t* out, int32_t* status, cudaStream_t stream,
+                         uint64_t wait_limit_ns);
+
+cudaError_t launch_bounded_wait_probe(int32_t* status, uint64_t limit_ns, cudaStream_t stream);
+
+}  // namespace pk

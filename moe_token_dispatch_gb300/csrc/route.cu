@@ -1,0 +1,230 @@
+// Routing kernels: expert histogram, exclusive scan and the stable
+// (expert, token, slot) permutation of the routed rows -- the "dispatch" half
+// of the token-dispatch + GEMM of "Loads and Loads of Fluffy Kittens"
+// ("Key claims", Fig. 17), restated for one device.
+//
+// The flat routing array topk_idx[T*k] is cut into chunks of kRouteChunk
+// entries, one block per chunk, in flat order. Workspace holds one row of E
+// counters per chunk:
+//   k_route_hist   row b = histogram of chunk b;
+//   k_route_scan   counts, offsets = exclusive scan of the column sums, and
+//                  row b rewritten in place to the first output position of
+//                  chunk b's entries of each expert:
+//                    base[b][e] = offsets[e] + sum_{b' < b} hist[b'][e];
+//   k_build_perm   each warp of block b owns a contiguous run of the chunk;
+//                  a per-warp histogram and a scan over warps give every warp
+//                  its first position per expert, then warps walk their runs
+//                  32 entries at a time and rank equal experts inside a warp
+//                  with __match_any_sync. Positions follow flat order, so the
+//                  result is unique and needs no atomics.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "pk_internal.h"
+#include "pk_ptx.cuh"
+
+namespace pk {
+
+__global__ void __launch_bounds__(kRouteThreads)
+    k_route_hist(const int32_t* __restrict__ topk, int32_t R, int32_t E,
+                 int32_t* __restrict__ blockcnt, int32_t* status) {
+    extern __shared__ int32_t hist[];
+    for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
+    __syncthreads();
+    const int64_t beg = static_cast<int64_t>(blockIdx.x) * kRouteChunk;
+    const int64_t end = min(beg + kRouteChunk, static_cast<int64_t>(R));
+    const uint32_t lane = threadIdx.x & 31;
+    bool bad = false;
+    for (int64_t base = beg; base < end; base += blockDim.x) {
+        const int64_t i = base + threadIdx.x;
+        int32_t e = -1;
+        if (i < end) {
+            e = __ldg(topk + i);
+            if (e < 0 || e >= E) {
+                bad = true;
+                e = -1;
+            }
+        }
+        const uint32_t peers = __match_any_sync(0xffffffffu, e);
+        if (e >= 0 && lane == static_cast<uint32_t>(__ffs(peers) - 1))
+            atomicAdd(&hist[e], __popc(peers));
+    }
+    if (bad) report(status, PK_ERR_BAD_INDEX);
+    __syncthreads();
+    int32_t* row = blockcnt + static_cast<int64_t>(blockIdx.x) * E;
+    for (int e = threadIdx.x; e < E; e += blockDim.x) row[e] = hist[e];
+}
+
+constexpr int kScanThreads = 1024;
+
+__global__ void __launch_bounds__(kScanThreads)
+    k_route_scan(int32_t* __restrict__ blockcnt, int32_t nblk, int32_t E, int32_t* counts,
+                 int32_t* __restrict__ offsets) {
+    extern __shared__ int32_t sm[];
+    int32_t* tot = sm;            // [E]
+    int32_t* offs = sm + E;       // [E]
+    int32_t* wsum = sm + 2 * E;   // [32]
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+
+    for (int e = tid; e < E; e += blockDim.x) {
+        int32_t s = 0;
+        for (int b = 0; b < nblk; ++b) s += blockcnt[static_cast<int64_t>(b) * E + e];
+        tot[e] = s;
+        if (counts) counts[e] = s;
+    }
+    __syncthreads();
+
+    // Exclusive scan of tot[0, E): each thread sums `per` consecutive totals,
+    // a warp shuffle scan and a scan of the 32 warp sums combine them.
+    const int per = (E + kScanThreads - 1) / kScanThreads;
+    const int b0 = min(tid * per, E), b1 = min(b0 + per, E);
+    int32_t local = 0;
+    for (int i = b0; i < b1; ++i) local += tot[i];
+    int32_t incl = local;
+    for (int d = 1; d < 32; d <<= 1) {
+        const int32_t v = __shfl_up_sync(0xffffffffu, incl, d);
+        if (lane >= d) incl += v;
+    }
+    if (lane == 31) wsum[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        int32_t w = wsum[lane];
+        for (int d = 1; d < 32; d <<= 1) {
+            const int32_t v = __shfl_up_sync(0xffffffffu, w, d);
+            if (lane >= d) w += v;
+        }
+        wsum[lane] = w;  // inclusive over warps
+    }
+    __syncthreads();
+    int32_t run = (warp > 0 ? wsum[warp - 1] : 0) + incl - local;
+    for (int i = b0; i < b1; ++i) {
+        offs[i] = run;
+        offsets[i] = run;
+        run += tot[i];
+    }
+    if (tid == kScanThreads - 1) offsets[E] = wsum[31];
+    __syncthreads();
+
+    // Per-chunk starting positions, in place over the chunk histograms.
+    for (int e = tid; e < E; e += blockDim.x) {
+        int32_t r = offs[e];
+        for (int b = 0; b < nblk; ++b) {
+            int32_t* p = blockcnt + static_cast<int64_t>(b) * E + e;
+            const int32_t c = *p;
+            *p = r;
+            r += c;
+        }
+    }
+}
+
+__global__ void __launch_bounds__(kRouteThreads)
+    k_build_perm(const int32_t* __restrict__ topk, int32_t R, int32_t E,
+                 const int32_t* __restrict__ blockbase, int32_t* __restrict__ perm,
+                 int32_t* __restrict__ inv_perm, int32_t* status) {
+    extern __shared__ int32_t wpos[];  // [kRouteWarps][E]
+    constexpr int kPerWarp = kRouteChunk / kRouteWarps;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const uint32_t lt_mask = (1u << lane) - 1u;
+    for (int i = threadIdx.x; i < kRouteWarps * E; i += blockDim.x) wpos[i] = 0;
+    __syncthreads();
+
+    const int64_t wbeg = static_cast<int64_t>(blockIdx.x) * kRouteChunk +
+                         static_cast<int64_t>(warp) * kPerWarp;
+    const int64_t wend = min(wbeg + kPerWarp, static_cast<int64_t>(R));
+    int32_t* my = wpos + warp * E;
+
+    // Pass 1: histogram of this warp's run.
+    for (int64_t base = wbeg; base < wbeg + kPerWarp; base += 32) {
+        const int64_t i = base + lane;
+        int32_t e = -1;
+        if (i < wend) {
+            e = __ldg(topk + i);
+            if (e < 0 || e >= E) e = -1;
+        }
+        const uint32_t peers = __match_any_sync(0xffffffffu, e);
+        if (e >= 0 && lane == __ffs(peers) - 1) my[e] += __popc(peers);
+        __syncwarp();
+    }
+    __syncthreads();
+
+    // Pass 2: first position of every warp's entries, per expert.
+    const int32_t* bb = blockbase + static_cast<int64_t>(blockIdx.x) * E;
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        int32_t r = bb[e];
+        for (int w = 0; w < kRouteWarps; ++w) {
+            const int32_t c = wpos[w * E + e];
+            wpos[w * E + e] = r;
+            r += c;
+        }
+    }
+    __syncthreads();
+
+    // Pass 3: scatter in flat order.
+    bool bad = false;
+    for (int64_t base = wbeg; base < wbeg + kPerWarp; base += 32) {
+        const int64_t i = base + lane;
+        int32_t e = -1;
+        if (i < wend) {
+            e = __ldg(topk + i);
+            if (e < 0 || e >= E) e = -1;
+        }
+        const uint32_t peers = __match_any_sync(0xffffffffu, e);
+        if (e >= 0) {
+            const int32_t pos = my[e] + __popc(peers & lt_mask);
+            if (pos >= 0 && pos < R) {
+                perm[pos] = static_cast<int32_t>(i);
+                if (inv_perm) inv_perm[i] = pos;
+            } else {
+                bad = true;
+            }
+        }
+        __syncwarp();
+        if (e >= 0 && lane == __ffs(peers) - 1) my[e] += __popc(peers);
+        __syncwarp();
+    }
+    if (bad) report(status, PK_ERR_BAD_INDEX);
+}
+
+namespace {
+int g_perm_smem_set[64] = {0};
+}
+
+cudaError_t launch_route_counts(const int32_t* topk, int32_t R, int32_t E, int32_t* counts,
+                                int32_t* offsets, int32_t* blockbase, int32_t* status,
+                                cudaStream_t stream) {
+    const int nblk = route_blocks(R);
+    if (nblk > 0) {
+        k_route_hist<<<nblk, kRouteThreads, sizeof(int32_t) * E, stream>>>(topk, R, E, blockbase,
+                                                                           status);
+        cudaError_t err = cudaGetLastError();
+        if (err != cudaSuccess) return err;
+    }
+    k_route_scan<<<1, kScanThreads, sizeof(int32_t) * (2 * E + 32), stream>>>(blockbase, nblk, E,
+                                                                             counts, offsets);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_build_perm(const int32_t* topk, int32_t R, int32_t E,
+                              const int32_t* blockbase, int32_t* perm, int32_t* inv_perm,
+                              int32_t* status, cudaStream_t stream) {
+    const int nblk = route_blocks(R);
+    if (nblk == 0) return cudaSuccess;
+    const size_t smem = sizeof(int32_t) * kRouteWarps * static_cast<size_t>(E);
+    if (smem > 48 * 1024) {
+        int dev = 0;
+        cudaError_t err = cudaGetDevice(&dev);
+        if (err != cudaSuccess) return err;
+        if (dev < 0 || dev >= 64 || !g_perm_smem_set[dev]) {
+            err = cudaFuncSetAttribute(k_build_perm, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(sizeof(int32_t) * kRouteWarps *
+                                                        PK_MAX_EXPERTS));
+            if (err != cudaSuccess) return err;
+            if (dev >= 0 && dev < 64) g_perm_smem_set[dev] = 1;
+        }
+    }
+    k_build_perm<<<nblk, kRouteThreads, smem, stream>>>(topk, R, E, blockbase, perm, inv_perm,
+                                                       status);
+    return cudaGetLastError();
+}
+
+}  // namespace pk

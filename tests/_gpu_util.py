@@ -1,0 +1,103 @@
+"""Helpers shared by the GPU parity tests (not collected as a test module)."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import inputgen as ig
+import oracle
+
+# Element-wise GEMM tolerance against the float64 oracle.
+ATOL = 2e-2
+RTOL = 1e-2
+
+
+def u16_to_bf16_dev(a: np.ndarray) -> torch.Tensor:
+    a = np.ascontiguousarray(a, dtype=np.uint16)
+    return torch.from_numpy(a.view(np.int16)).cuda().view(torch.bfloat16)
+
+
+def bf16_dev_to_f64(t: torch.Tensor) -> np.ndarray:
+    bits = t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+    return ig.bf16_bits_to_f64(bits)
+
+
+def run_gpu(pk, x_u16, topk, W_dev, E, De, x_dev=None):
+    """Runs the three C-ABI calls; returns numpy copies of every output."""
+    T, k = topk.shape
+    D = x_u16.shape[1]
+    md = pk.MoeDispatch(T, k, E, D, De)
+    x = x_dev if x_dev is not None else u16_to_bf16_dev(x_u16)
+    tk = torch.from_numpy(np.ascontiguousarray(topk, dtype=np.int32)).cuda()
+    md.route(tk)
+    md.gemm(x, W_dev)
+    torch.cuda.synchronize()
+    R = T * k
+    return {
+        "counts": md.counts.cpu().numpy(),
+        "offsets": md.offsets.cpu().numpy(),
+        "perm": md.perm[:R].cpu().numpy(),
+        "inv_perm": md.inv_perm[:R].cpu().numpy(),
+        "out_dev": md.out[:R],
+        "status": md.status_code(),
+        "md": md,
+    }
+
+
+def assert_indices_exact(res, ref):
+    assert np.array_equal(res["counts"].astype(np.int64), ref["counts"])
+    assert np.array_equal(res["offsets"].astype(np.int64), ref["offsets"])
+    assert np.array_equal(res["perm"].astype(np.int64), ref["perm"])
+    assert np.array_equal(res["inv_perm"].astype(np.int64), ref["inv_perm"])
+
+
+def assert_gemm_close(gpu_rows: np.ndarray, ref_rows: np.ndarray, rows=None):
+    err = np.abs(gpu_rows - ref_rows)
+    bound = ATOL + RTOL * np.abs(ref_rows)
+    bad = err > bound
+    if bad.any():
+        i, n = np.argwhere(bad)[0]
+        r = rows[i] if rows is not None else i
+        raise AssertionError(
+            f"{int(bad.sum())} of {bad.size} elements outside |gpu-ref| <= {ATOL} + {RTOL}|ref|; "
+            f"first at row {r} col {n}: gpu={gpu_rows[i, n]!r} ref={ref_rows[i, n]!r}")
+    assert np.isfinite(gpu_rows).all()
+
+
+def boundary_rows(offsets: np.ndarray, rng, n_random: int = 64, per_expert=True) -> np.ndarray:
+    """First/last rows of every expert, rows at 128-row tile edges, random rows."""
+    R = int(offsets[-1])
+    rows = set()
+    E = offsets.size - 1
+    for e in range(E):
+        lo, hi = int(offsets[e]), int(offsets[e + 1])
+        if hi <= lo:
+            continue
+        rows.update((lo, hi - 1))
+        if per_expert:
+            for b in (31, 32, 127, 128, 255, 256, 257, 383, 384, 511, 512):
+                if lo + b < hi:
+                    rows.add(lo + b)
+    if R:
+        rows.update(int(v) for v in rng.integers(0, R, size=n_random))
+    return np.array(sorted(rows), dtype=np.int64)
+
+
+def check_case(pk, x_u16, topk, W_u16, E, rows=None, W_dev=None, threads=None):
+    """Full parity check of one case; GEMM on `rows` (all rows when None)."""
+    De = W_u16.shape[2]
+    if W_dev is None:
+        W_dev = u16_to_bf16_dev(W_u16)
+    res = run_gpu(pk, x_u16, topk, W_dev, E, De)
+    assert res["status"] == 0, pk.pk_status_str(res["status"])
+    ref = oracle.run(topk, E)
+    assert_indices_exact(res, ref)
+    R = topk.size
+    if rows is None:
+        rows = np.arange(R, dtype=np.int64)
+    if len(rows):
+        want = oracle.gemm_rows(x_u16, ref["perm"], ref["offsets"], W_u16, topk.shape[1], rows,
+                                threads)
+        got = bf16_dev_to_f64(res["out_dev"][torch.from_numpy(rows).cuda()])
+        assert_gemm_close(got, want, rows)
+    return res, ref

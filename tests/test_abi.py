@@ -1,0 +1,105 @@
+"""The C ABI library loads, exports every declared entry point, and rejects
+bad arguments on the host (CPU only: no call here reaches the device)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "pk_moe.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from moe_token_dispatch_gb300 import _build
+    _build.build()
+    import moe_token_dispatch_gb300 as pk
+    return pk
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"\b(pk_[a-z0-9_]+)\s*\(", text)
+    return sorted(set(names))
+
+
+def test_header_declares_the_path():
+    names = declared_functions()
+    for n in ("pk_moe_route_counts", "pk_moe_build_perm", "pk_moe_dispatch_gemm",
+              "pk_moe_workspace_bytes", "pk_status_str"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    so = ctypes.CDLL(lib.LIB_PATH)
+    for name in declared_functions():
+        assert hasattr(so, name), name
+
+
+def test_status_strings(lib):
+    assert lib.pk_status_str(0) == "PK_OK"
+    assert lib.pk_status_str(lib.PK_ERR_TIMEOUT) == "PK_ERR_TIMEOUT"
+    assert lib.pk_status_str(99) == "PK_ERR_UNKNOWN"
+    assert lib.pk_abi_version() >= 10000
+
+
+def test_workspace_bytes(lib):
+    assert lib.pk_moe_workspace_bytes(0, 8, 256) == 0
+    # 2048 routed entries per block, E int32 counters per block, 256-byte rounding
+    assert lib.pk_moe_workspace_bytes(8192, 8, 256) == 32 * 256 * 4
+    assert lib.pk_moe_workspace_bytes(1, 1, 3) == 256
+    assert lib.pk_moe_workspace_bytes(2049, 1, 64) == 2 * 64 * 4
+    assert lib.pk_moe_workspace_bytes(2049, 1, 5) == 256
+
+
+def _raw(lib):
+    return lib.lib
+
+
+FAKE = ctypes.c_void_p(0x10000)       # never dereferenced: every call below fails its checks
+FAKE_ODD = ctypes.c_void_p(0x10008)   # not 16-byte aligned
+
+
+@pytest.mark.parametrize("args,code", [
+    ((FAKE, -1, 2, 8, None, FAKE, FAKE, 4096, None, None), 1),   # T < 0
+    ((FAKE, 4, 0, 8, None, FAKE, FAKE, 4096, None, None), 1),    # k < 1
+    ((FAKE, 4, 9, 8, None, FAKE, FAKE, 4096, None, None), 1),    # k > E
+    ((FAKE, 4, 2, 8, None, None, FAKE, 4096, None, None), 1),    # no offsets
+    ((FAKE, 4, 2, 5000, None, FAKE, FAKE, 1 << 20, None, None), 2),  # E too large
+    ((FAKE, 4, 2, 8, None, FAKE, FAKE, 16, None, None), 1),      # workspace too small
+    ((FAKE, 4, 2, 8, None, FAKE, FAKE_ODD, 4096, None, None), 1),  # workspace misaligned
+    ((FAKE, 1 << 29, 8, 8, None, FAKE, FAKE, 1 << 40, None, None), 2),  # T*k >= 2^31
+])
+def test_route_counts_rejects(lib, args, code):
+    assert _raw(lib).pk_moe_route_counts(*args) == code
+
+
+@pytest.mark.parametrize("args,code", [
+    ((FAKE, FAKE, FAKE, FAKE, 4, 2, 7, 8, 64, FAKE, None, None), 1),     # D % 8
+    ((FAKE, FAKE, FAKE, FAKE, 4, 2, 64, 8, 12, FAKE, None, None), 1),    # De % 8
+    ((FAKE_ODD, FAKE, FAKE, FAKE, 4, 2, 64, 8, 64, FAKE, None, None), 1),  # x misaligned
+    ((FAKE, FAKE, FAKE, FAKE_ODD, 4, 2, 64, 8, 64, FAKE, None, None), 1),  # W misaligned
+    ((FAKE, FAKE, FAKE, FAKE, 4, 2, 64, 8, 64, FAKE_ODD, None, None), 1),  # out misaligned
+    ((FAKE, None, FAKE, FAKE, 4, 2, 64, 8, 64, FAKE, None, None), 1),    # no perm
+    ((FAKE, FAKE, FAKE, FAKE, 4, 0, 64, 8, 64, FAKE, None, None), 1),    # k < 1
+    ((FAKE, FAKE, FAKE, FAKE, 1 << 29, 8, 64, 8, 64, FAKE, None, None), 2),  # T*k >= 2^31
+])
+def test_dispatch_gemm_rejects(lib, args, code):
+    assert _raw(lib).pk_moe_dispatch_gemm(*args) == code
+
+
+def test_zero_rows_are_a_no_op(lib):
+    # T == 0: nothing to launch for build_perm and dispatch_gemm
+    assert _raw(lib).pk_moe_build_perm(None, 0, 2, 8, None, None, None, None, 0, None, None) == 0
+    assert _raw(lib).pk_moe_dispatch_gemm(None, None, None, None, 0, 2, 64, 8, 64, None, None,
+                                          None) == 0
+
+
+def test_build_perm_rejects(lib):
+    assert _raw(lib).pk_moe_build_perm(FAKE, 4, 2, 8, FAKE, None, None, FAKE, 4096, None,
+                                       None) == 1
+    assert _raw(lib).pk_moe_build_perm(FAKE, 4, 2, 8, FAKE, FAKE, None, FAKE, 8, None,
+                                       None) == 1
+    assert _raw(lib).pk_debug_bounded_wait(None, 10, None) == 1

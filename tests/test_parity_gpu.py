@@ -1,0 +1,169 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle.
+
+Indices (counts, offsets, perm, inv_perm) must match bit for bit. GEMM
+outputs must satisfy |gpu - ref| <= 2e-2 + 1e-2 |ref| element-wise against
+the float64 oracle.
+"""
+import numpy as np
+import pytest
+import torch
+
+import inputgen as ig
+import oracle
+from _gpu_util import (assert_gemm_close, bf16_dev_to_f64, boundary_rows, check_case,
+                       run_gpu, u16_to_bf16_dev)
+
+pytestmark = pytest.mark.gpu
+
+
+def _case(T, D, E, k, De, zipf=0.0, seed=0):
+    wl = ig.custom(T=T, D=D, E=E, k=k, De=De, zipf_s=zipf, seed=seed)
+    c = ig.make_case(wl)
+    return c.x, c.topk, c.W
+
+
+def test_tiny_workload_all_rows(gpu_lib):
+    wl = ig.WORKLOADS["tiny"]
+    c = ig.make_case(wl)
+    check_case(gpu_lib, c.x, c.topk, c.W, wl.E)
+
+
+# Several tiles in every direction and ragged tails, small enough for the
+# oracle to do every row: m-tiles per expert 1..6 (two-m-tile units and
+# several groups), n-tiles of 256 + a ragged one, K-steps past the 3-stage
+# ring, K and N not multiples of 64.
+MULTI_TILE = [
+    # T,   D,   E, k,  De
+    (512, 576, 4, 2, 640),      # ~256 rows/expert, 9 K-steps, N tail 128
+    (700, 200, 3, 1, 200),      # D and De not multiples of 64
+    (300, 1024, 8, 3, 1408),    # mid-like widths, 16 K-steps
+    (1000, 64, 2, 2, 256),      # 1000 rows per expert: 8 m-tiles, 4 groups
+    (96, 8, 5, 2, 8),           # smallest legal D and De
+]
+
+
+@pytest.mark.parametrize("T,D,E,k,De", MULTI_TILE)
+def test_multi_tile_all_rows(gpu_lib, T, D, E, k, De):
+    x, topk, W = _case(T, D, E, k, De)
+    check_case(gpu_lib, x, topk, W, E)
+
+
+def test_single_token_single_expert(gpu_lib):
+    x, topk, W = _case(1, 64, 1, 1, 64)
+    check_case(gpu_lib, x, topk, W, 1)
+
+
+def test_empty_experts_and_one_expert_takes_all(gpu_lib):
+    T, D, E, k, De = 333, 128, 16, 1, 192
+    x, _, W = _case(T, D, E, k, De)
+    topk = np.full((T, k), 7, dtype=np.int32)
+    res, ref = check_case(gpu_lib, x, topk, W, E)
+    assert res["counts"].tolist() == [0] * 7 + [T] + [0] * 8
+
+
+def test_duplicate_experts_in_one_token(gpu_lib):
+    T, D, E, k, De = 77, 64, 4, 3, 64
+    x, _, W = _case(T, D, E, k, De)
+    rng = np.random.default_rng(11)
+    topk = rng.integers(0, E, size=(T, k)).astype(np.int32)
+    topk[:5] = 2  # all three slots of the first tokens to one expert
+    check_case(gpu_lib, x, topk, W, E)
+
+
+def test_skewed_routing_small(gpu_lib):
+    x, topk, W = _case(2048, 256, 32, 4, 384, zipf=1.2)
+    counts = np.bincount(topk.ravel(), minlength=32)
+    assert counts.max() > 4 * counts.mean()
+    check_case(gpu_lib, x, topk, W, 32)
+
+
+def test_zero_tokens(gpu_lib):
+    pk = gpu_lib
+    md = pk.MoeDispatch(0, 2, 8, 64, 64)
+    md.offsets.fill_(-7)
+    md.counts.fill_(-7)
+    tk = torch.zeros((0, 2), dtype=torch.int32, device="cuda")
+    md.route(tk)
+    x = torch.zeros((0, 64), dtype=torch.bfloat16, device="cuda")
+    W = torch.zeros((8, 64, 64), dtype=torch.bfloat16, device="cuda")
+    md.gemm(x, W)
+    torch.cuda.synchronize()
+    assert md.offsets.tolist() == [0] * 9 and md.counts.tolist() == [0] * 8
+
+
+def test_bad_index_sets_status(gpu_lib):
+    pk = gpu_lib
+    T, k, E = 40, 2, 4
+    topk = np.random.default_rng(1).integers(0, E, size=(T, k)).astype(np.int32)
+    topk[3, 1] = E  # out of range
+    topk[9, 0] = -1
+    md = pk.MoeDispatch(T, k, E, 64, 64)
+    md.route(torch.from_numpy(topk).cuda())
+    torch.cuda.synchronize()
+    assert md.status_code() == pk.PK_ERR_BAD_INDEX
+    # the valid entries are still counted
+    valid = topk[(topk >= 0) & (topk < E)]
+    assert md.counts.cpu().numpy().tolist() == np.bincount(valid, minlength=E).tolist()
+
+
+def test_repeat_runs_are_bitwise_identical(gpu_lib):
+    x, topk, W = _case(512, 576, 4, 2, 640)
+    Wd = u16_to_bf16_dev(W)
+    a = run_gpu(gpu_lib, x, topk, Wd, 4, 640)
+    b = run_gpu(gpu_lib, x, topk, Wd, 4, 640)
+    assert torch.equal(a["out_dev"].view(torch.int16), b["out_dev"].view(torch.int16))
+    assert np.array_equal(a["perm"], b["perm"])
+
+
+def test_bounded_wait_times_out_and_context_survives(gpu_lib):
+    pk = gpu_lib
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record()
+    pk.pk_debug_bounded_wait(st, 50_000_000)  # 50 ms
+    t1.record()
+    torch.cuda.synchronize()
+    assert st.item() == pk.PK_ERR_TIMEOUT
+    assert t0.elapsed_time(t1) >= 40.0
+    # the context still works
+    x, topk, W = _case(64, 64, 2, 1, 64)
+    check_case(pk, x, topk, W, 2)
+
+
+# ------------------------------------------------- the five named workloads
+def test_mid_workload(gpu_lib):
+    wl = ig.WORKLOADS["mid"]
+    c = ig.make_case(wl)
+    rows = boundary_rows(oracle.route_counts(c.topk, wl.E)[1], np.random.default_rng(0), 256)
+    check_case(gpu_lib, c.x, c.topk, c.W, wl.E, rows=rows)
+
+
+@pytest.fixture(scope="module")
+def big_W():
+    """W for D=7168, E=256, D_expert=2048 (7.5 GB), shared by the three
+    full-size workloads, which use the same seed and shape."""
+    wl = ig.WORKLOADS["ep"]
+    W = ig.make_W(wl)
+    Wd = u16_to_bf16_dev(W)
+    yield W, Wd
+    del Wd
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", ["ep", "skew", "decode"])
+def test_full_size_workloads(gpu_lib, big_W, name):
+    wl = ig.WORKLOADS[name]
+    W, Wd = big_W
+    x = ig.make_x(wl)
+    topk = ig.make_topk(wl)
+    offsets = oracle.route_counts(topk, wl.E)[1]
+    rows = boundary_rows(offsets, np.random.default_rng(1), 128)
+    res, ref = check_case(gpu_lib, x, topk, W, wl.E, rows=rows, W_dev=Wd)
+    out = res["out_dev"]
+    # every row of the output, not only the sampled ones, is finite
+    assert bool(torch.isfinite(out.float()).all())
+    if name == "skew":
+        counts = ref["counts"]
+        assert (counts == 0).sum() > 20 and counts.max() > 2000
