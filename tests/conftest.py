@@ -19,7 +19,7 @@ def gpu_lib():
     import torch
     if not torch.cuda.is_available():
         pytest.fail("GPU test run without a CUDA device")
-    from moe_token_dispatch_gb300 import _build
-    _build.build()
+    import __graft_entry__
+    __graft_entry__._build_module().build()
     import moe_token_dispatch_gb300 as pk
     return pk

@@ -12,8 +12,8 @@ HEADER = os.path.join(ROOT, "include", "pk_moe.h")
 
 @pytest.fixture(scope="module")
 def lib():
-    from moe_token_dispatch_gb300 import _build
-    _build.build()
+    import __graft_entry__
+    __graft_entry__._build_module().build()
     import moe_token_dispatch_gb300 as pk
     return pk
 
