@@ -1,0 +1,440 @@
+#!/usr/bin/env python3
+"""Benchmark: MoE token dispatch + expert GEMM on GB300.
+
+One step = pk_moe_route_counts + pk_moe_build_perm + pk_moe_dispatch_gemm on
+one batch of seeded synthetic input (the expert-parallel shape of "Loads and
+Loads of Fluffy Kittens", "Key claims", Fig. 17: T=8192 tokens, D=7168,
+E=256 experts, top_k=8, D_expert=2048). Prints one JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload ep|skew|decode|mid|tiny]
+
+``--impl reference`` times the CPU oracle (float64, all host cores) on a
+bounded sample of the same workload. N > 1 (torchrun) runs one independent
+replica per GPU: the path has no cross-GPU step.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+METRIC = "dispatch+expert-GEMM TFLOP/s and % of GB300 BF16 peak at T=8192 D=7168 E=256 k=8"
+UNIT = "TFLOP/s"
+PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+GEMM_SOURCE = os.path.join(ROOT, "moe_token_dispatch_gb300", "csrc", "dispatch_gemm.cu")
+
+
+# --------------------------------------------------------------- utilities
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    except (OSError, ValueError):
+        return dict(PEAKS_FALLBACK), "fallback"
+
+
+def source_digest(path=GEMM_SOURCE) -> str:
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def profiled_traffic(workload: str):
+    """DRAM bytes per GEMM launch from the committed ncu summary, if it was
+    taken on the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", f"dispatch_gemm_{workload}.md")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    s = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", text)
+    if not m or not s or s.group(1) != source_digest():
+        return None
+    return float(m.group(1))
+
+
+def workload_bytes(wl, counts: np.ndarray) -> dict:
+    R = wl.T * wl.k
+    touched = int((counts > 0).sum())
+    return {
+        "x_gathered": R * wl.D * 2,
+        "w_touched": touched * wl.D * wl.De * 2,
+        "out": R * wl.De * 2,
+        "indices": R * 4 + (wl.E + 1) * 4,
+        "experts_touched": touched,
+    }
+
+
+def config_of(wl) -> dict:
+    return {
+        "workload": f"{wl.name}: T={wl.T} D={wl.D} E={wl.E} top_k={wl.k} D_expert={wl.De}"
+                    + (f" zipf_s={wl.zipf_s}" if wl.zipf_s else ""),
+        "T": wl.T, "D": wl.D, "E": wl.E, "top_k": wl.k, "D_expert": wl.De,
+        "routing": "top-k of N(0,1) router logits" + (f" + bias -{wl.zipf_s}*ln(e+1)" if wl.zipf_s else ""),
+        "x": "bf16 N(0,1)", "W": "bf16 N(0,1)/sqrt(D)", "seed": wl.seed,
+        "l2": f"inputs larger than L2: {wl.E * wl.D * wl.De * 2 / 1e9:.2f} GB of W streamed per step"
+              if wl.E * wl.D * wl.De * 2 > 256e6 else "L2 flushed (512 MB write) between steps",
+    }
+
+
+# ------------------------------------------------------------ distributed
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def max_over_ranks(value: float) -> float:
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return value
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 100 ms."""
+    FIELDS = ("uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_uuid: str | None):
+        self.samples = []
+        self.proc = None
+        self.uuid = (gpu_uuid or "").lower().replace("gpu-", "")
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+               "-lms", "100"]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), [c.strip() for c in line.split(",")]))
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0: float, t1: float) -> dict:
+        inside = [s for t, s in self.samples if t0 <= t <= t1 + 0.15 and len(s) >= 9
+                  and (not self.uuid or s[0].lower().replace("gpu-", "") == self.uuid)]
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for s in inside for n, v in zip(names, s[5:9]) if v == "Active"})
+
+        def num(v):
+            try:
+                return float(v)
+            except ValueError:
+                return None
+        sm = [num(s[1]) for s in inside if num(s[1]) is not None]
+        mx = [num(s[2]) for s in inside if num(s[2]) is not None]
+        pw = [num(s[3]) for s in inside if num(s[3]) is not None]
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "power_w_max": max(pw) if pw else None,
+                "reasons": reasons, "samples": len(inside)}
+
+
+# ------------------------------------------------------------ CPU oracle
+def oracle_sample(case, wl, seconds: float, threads: int):
+    """Times the oracle on a bounded sample: full routing plus the GEMM of a
+    sample of rows, sized to take about `seconds`. Returns (TFLOP/s, info)."""
+    import oracle
+    t0 = time.perf_counter()
+    counts, offsets = oracle.route_counts(case.topk, wl.E)
+    perm, _ = oracle.build_perm(case.topk, wl.E, offsets)
+    t_route = time.perf_counter() - t0
+    rng = np.random.default_rng(0)
+    R = wl.T * wl.k
+    # calibrate: one row per thread
+    probe = rng.integers(0, R, size=threads)
+    W = _ensure_w_rows(case, wl, offsets, probe)
+    t0 = time.perf_counter()
+    oracle.gemm_rows(case.x, perm, offsets, W, wl.k, probe, threads)
+    t_probe = time.perf_counter() - t0
+    per_row = t_probe / len(probe)
+    n = int(max(threads, min(R, (seconds - t_route) / max(per_row, 1e-9))))
+    rows = rng.integers(0, R, size=n)
+    W = _ensure_w_rows(case, wl, offsets, rows)
+    t0 = time.perf_counter()
+    oracle.gemm_rows(case.x, perm, offsets, W, wl.k, rows, threads)
+    t_gemm = time.perf_counter() - t0
+    flops = 2.0 * wl.D * wl.De * n
+    sec = t_route + t_gemm
+    return flops / sec / 1e12, {"rows": n, "seconds": sec, "route_s": t_route}
+
+
+def _ensure_w_rows(case, wl, offsets, rows):
+    """Fills (lazily) the experts of the given sorted rows in a sparse W."""
+    import inputgen as ig
+    if case.W is None:
+        case.W = np.zeros((wl.E, wl.D, wl.De), dtype=np.uint16)
+    ex = np.searchsorted(offsets, rows, side="right") - 1
+    for e in sorted(set(int(v) for v in ex)):
+        if e not in case.w_filled:
+            ig.fill_w_expert(wl, case.W, e)
+            case.w_filled.add(e)
+    return case.W
+
+
+# ----------------------------------------------------------------- arms
+def run_reference(args, wl):
+    import inputgen as ig
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return None
+    threads = os.cpu_count() or 1
+    case = ig.make_case(wl, with_W=False)
+    steps, warm = args.steps, args.warmup
+    per_step = max(0.05, min(2.0, 150.0 / (steps + warm)))
+    for _ in range(warm):
+        oracle_sample(case, wl, per_step, threads)
+    vals, rows, secs = [], 0, 0.0
+    for _ in range(steps):
+        v, info = oracle_sample(case, wl, per_step, threads)
+        vals.append(v)
+        rows += info["rows"]
+        secs += info["seconds"]
+    value = 2.0 * wl.D * wl.De * rows / secs / 1e12
+    sample = (f"per step: full routing of {wl.T * wl.k} entries + float64 GEMM of ~{rows // steps} "
+              f"random sorted rows (of {wl.T * wl.k}), {steps} steps")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+        "n_gpus": world, "steps": steps, "warmup": warm,
+        "ms_per_step": 1000.0 * secs / steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": config_of(wl),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    return line
+
+
+def run_ours(args, wl):
+    import torch
+    import inputgen as ig
+    import moe_token_dispatch_gb300 as pk
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream()
+
+    case = ig.make_case(wl, with_W=True)
+    W_host = case.W
+
+    def to_dev(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
+
+    x = to_dev(case.x)
+    W = to_dev(W_host)
+    topk = torch.from_numpy(case.topk).to(dev)
+    md = pk.MoeDispatch(wl.T, wl.k, wl.E, wl.D, wl.De, device=dev, with_inv_perm=True)
+    R = wl.T * wl.k
+    flops = 2.0 * R * wl.D * wl.De
+    flush = None
+    if wl.E * wl.D * wl.De * 2 <= 256e6:
+        flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
+
+    def step(ev=None):
+        md.route(topk, stream)
+        if ev is not None:
+            ev[0].record(stream)
+        md.gemm(x, W, stream)
+        if ev is not None:
+            ev[1].record(stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+        if flush is not None:
+            flush.fill_(1)
+    torch.cuda.synchronize()
+    if md.status_code() != 0:
+        raise RuntimeError(f"device status {pk.pk_status_str(md.status_code())}")
+    counts = md.counts.cpu().numpy()
+
+    try:
+        gpu_uuid = str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        gpu_uuid = None
+    sampler = ClockSampler(gpu_uuid) if rank == 0 else None
+    time.sleep(0.3 if sampler else 0)
+
+    K = args.steps
+    gemm_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(K)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    flush_ms = 0.0
+    barrier()
+    torch.cuda.synchronize()
+    wall0 = time.time()
+    start.record(stream)
+    for i in range(K):
+        step(gemm_ev[i])
+        if flush is not None:
+            flush.fill_(1)
+    end.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    wall1 = time.time()
+    total_ms = start.elapsed_time(end)
+    gemm_ms = [a.elapsed_time(b) for a, b in gemm_ev]
+    if flush is not None:
+        f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        f0.record(stream)
+        flush.fill_(1)
+        f1.record(stream)
+        torch.cuda.synchronize()
+        flush_ms = f0.elapsed_time(f1) * K
+        total_ms = max(total_ms - flush_ms, 1e-6)
+    if md.status_code() != 0:
+        raise RuntimeError(f"device status {pk.pk_status_str(md.status_code())}")
+    step_ms = max_over_ranks(total_ms / K)
+    gemm_avg_ms = max_over_ranks(sum(gemm_ms) / K)
+
+    # ---- end to end through the public API, host buffers, copies timed
+    x_h = torch.from_numpy(np.ascontiguousarray(case.x).view(np.int16)).view(torch.bfloat16).pin_memory()
+    tk_h = torch.from_numpy(case.topk).pin_memory()
+    out_h = torch.empty((R, wl.De), dtype=torch.bfloat16).pin_memory()
+    x_d = torch.empty_like(x)
+    tk_d = torch.empty_like(topk)
+    Ke = max(1, min(K, 200))
+
+    def e2e_step():
+        x_d.copy_(x_h, non_blocking=True)
+        tk_d.copy_(tk_h, non_blocking=True)
+        md.route(tk_d, stream)
+        md.gemm(x_d, W, stream)
+        out_h.copy_(md.out[:R], non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(Ke):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / Ke)
+
+    if sampler:
+        sampler.stop()
+    if rank != 0:
+        return None
+
+    peaks, peak_kind = load_peaks()
+    b = workload_bytes(wl, counts)
+    alg_bytes = b["x_gathered"] + b["w_touched"] + b["out"] + b["indices"]
+    achieved_gbs = alg_bytes / (gemm_avg_ms * 1e-3) / 1e9
+    gemm_tflops = flops / (gemm_avg_ms * 1e-3) / 1e12
+    value = world * flops / (step_ms * 1e-3) / 1e12
+    traffic = profiled_traffic(wl.name)
+
+    cpu_value, cpu_info = oracle_sample(case, wl, args.cpu_seconds, os.cpu_count() or 1)
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": max(3, args.warmup), "ms_per_step": step_ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": config_of(wl),
+        "pct_bf16_peak": 100.0 * value / world / peaks["bf16_tflops"],
+        "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": peaks["hbm_gbs"],
+                     "unit": "GB/s", "frac": achieved_gbs / peaks["hbm_gbs"],
+                     "traffic": traffic, "peak_kind": peak_kind,
+                     "kernel": "k_dispatch_gemm", "kernel_ms": gemm_avg_ms,
+                     "algorithmic_bytes": alg_bytes, "bytes_breakdown": b,
+                     "tensor": {"achieved": gemm_tflops, "peak": peaks["bf16_tflops"],
+                                "peak_sustained": peaks.get("bf16_tflops_sustained"),
+                                "unit": "TFLOP/s", "frac": gemm_tflops / peaks["bf16_tflops"]}},
+        "kernel_share": {"k_dispatch_gemm": gemm_avg_ms / step_ms},
+        "cpu_baseline": {"value": cpu_value, "unit": UNIT, "cores": os.cpu_count() or 1,
+                         "kind": "oracle",
+                         "sample": f"full routing + float64 GEMM of {cpu_info['rows']} random "
+                                   f"sorted rows of {R} ({cpu_info['seconds']:.1f} s)"},
+        "e2e": {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
+                "h2d_bytes_per_step": x.numel() * 2 + topk.numel() * 4,
+                "d2h_bytes_per_step": R * wl.De * 2, "ms_per_step": e2e_ms,
+                "note": "x and topk_idx copied in from pinned host memory and out copied back "
+                        "every step; W stays resident (layer weights)"},
+        "gpu_launches": 4 * K,
+        "clocks": sampler.summary(wall0, wall1) if sampler else None,
+    }
+    return line
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="ep")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    args = ap.parse_args(argv)
+    args.warmup = max(3, args.warmup)
+
+    import inputgen as ig
+    wl = ig.WORKLOADS[args.workload]
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        if args.impl == "ours":
+            import torch
+            torch.cuda.set_device(local)
+            dist.init_process_group("nccl")
+        else:
+            if rank != 0:
+                return 0
+    if args.impl == "reference":
+        line = run_reference(args, wl)
+    else:
+        line = run_ours(args, wl)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+    if world > 1 and args.impl == "ours":
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

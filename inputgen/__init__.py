@@ -154,6 +154,11 @@ WORKLOADS = {
                      desc="same shape, router logits biased by -1.2*ln(e+1) (Zipf s=1.2)"),
     "decode": Workload("decode", 128, 7168, 256, 8, 2048,
                        desc="decode-like: 128 tokens, weight-bound"),
+    # profiling case: the "ep" shape cut to 32 experts and 1024 tokens, so
+    # rows per expert (~256) and every tile shape stay those of "ep" while
+    # W (0.94 GB) still exceeds L2
+    "ep32": Workload("ep32", 1024, 7168, 32, 8, 2048,
+                     desc="ep shape with 32 experts and 1024 tokens (profiling size)"),
 }
 
 

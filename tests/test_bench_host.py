@@ -1,0 +1,70 @@
+"""Host-side logic of bench.py (CPU only): max-over-ranks timing with two
+gloo ranks, the byte accounting and the JSON line of the reference arm."""
+import os
+import socket
+
+import numpy as np
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+import bench
+import inputgen as ig
+
+
+def _free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    return port
+
+
+def _worker(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        v = bench.max_over_ranks(1.5 + rank)   # rank 1 is the slow one
+        bench.barrier()
+        q.put((rank, v))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_max_over_ranks_two_gloo_ranks():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(120)
+        assert p.exitcode == 0
+    got = dict(q.get(timeout=10) for _ in range(2))
+    assert got == {0: 2.5, 1: 2.5}
+
+
+def test_single_process_max_is_identity():
+    assert bench.max_over_ranks(3.25) == 3.25
+
+
+def test_workload_bytes_counts_only_touched_experts():
+    wl = ig.custom(T=4, D=16, E=5, k=2, De=8)
+    counts = np.array([3, 0, 5, 0, 0])
+    b = bench.workload_bytes(wl, counts)
+    assert b["experts_touched"] == 2
+    assert b["w_touched"] == 2 * 16 * 8 * 2
+    assert b["x_gathered"] == 8 * 16 * 2 and b["out"] == 8 * 8 * 2
+
+
+def test_reference_arm_line(capsys):
+    # the tiny workload keeps this fast; the line keeps the contract's keys
+    bench.main(["--impl", "reference", "--workload", "tiny", "--steps", "2", "--warmup", "3"])
+    import json
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["unit"] == "TFLOP/s"
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["value"] > 0
+    assert line["steps"] == 2 and line["warmup"] == 3
