@@ -131,6 +131,33 @@ int pk_moe_dispatch_gemm(const uint16_t* x, const int32_t* perm, const int32_t* 
                          int32_t D_expert, uint16_t* out, int32_t* status_word, void* stream);
 
 /*
+ * Routing without any device allocation (the pages have no counterpart: this
+ * is an interface convenience, not a step of the method). Computes exactly
+ * what pk_moe_route_counts followed by pk_moe_build_perm compute (counts,
+ * offsets, perm, inv_perm), for callers that cannot call cudaMalloc -- a host
+ * program that hands all device memory to its own pool at start-up, a plug-in
+ * that may not bypass its host runtime's allocator, or a latency-critical path
+ * that cannot afford cudaMalloc's implicit synchronisation -- and therefore
+ * cannot provide a workspace.
+ *   The per-chunk counters live in a fixed array of PK_NOALLOC_SCRATCH_BYTES
+ * inside the library's device image, held by every GPU that loads the library
+ * until the process exits. Sizes with ceil(T*k / 2048) * E * 4 bytes above
+ * that limit are rejected with PK_ERR_UNSUPPORTED (E = 256 allows T*k up to
+ * 2,097,152). The call allocates nothing and calls no cudaMalloc/cudaFree.
+ *   The first call on each device looks up the array's device address with
+ * that device current; make that first call before any stream capture. Every
+ * call shares the one array and leaves its contents behind; each call rewrites
+ * every counter it reads, so nothing needs clearing, but calls that overlap on
+ * the GPU (other streams or host threads) race: order them on one stream.
+ *   Arguments, layouts and status reporting as for pk_moe_route_counts and
+ * pk_moe_build_perm (expert_counts and inv_perm may be NULL).
+ */
+#define PK_NOALLOC_SCRATCH_BYTES (1u << 20)
+int pk_moe_route_noalloc(const int32_t* topk_idx, int32_t T, int32_t k, int32_t E,
+                         int32_t* expert_counts, int32_t* expert_offsets, int32_t* perm,
+                         int32_t* inv_perm, int32_t* status_word, void* stream);
+
+/*
  * Limit, in nanoseconds, on every pipeline wait inside the GEMM kernel
  * (default 4e9). A wait that runs out sets PK_ERR_TIMEOUT and the kernel
  * drains its own copies and returns. Applies to later launches from this

@@ -15,6 +15,7 @@ from ._binding import (  # noqa: F401
     PK_ERR_TIMEOUT,
     PK_ERR_UNSUPPORTED,
     PK_MAX_EXPERTS,
+    PK_NOALLOC_SCRATCH_BYTES,
     PK_OK,
     PkError,
     lib,
@@ -23,6 +24,7 @@ from ._binding import (  # noqa: F401
     pk_moe_build_perm,
     pk_moe_dispatch_gemm,
     pk_moe_route_counts,
+    pk_moe_route_noalloc,
     pk_moe_set_wait_limit_ns,
     pk_moe_workspace_bytes,
     pk_status_str,

@@ -21,6 +21,7 @@ PK_ERR_CUDA = 3
 PK_ERR_TIMEOUT = 4
 PK_ERR_BAD_INDEX = 5
 PK_MAX_EXPERTS = 4096
+PK_NOALLOC_SCRATCH_BYTES = 1 << 20
 
 
 class PkError(RuntimeError):
@@ -47,6 +48,8 @@ def _load():
     lib.pk_moe_build_perm.argtypes = [P, I32, I32, I32, P, P, P, P, SZ, P, P]
     lib.pk_moe_dispatch_gemm.restype = ctypes.c_int
     lib.pk_moe_dispatch_gemm.argtypes = [P, P, P, P, I32, I32, I32, I32, I32, P, P, P]
+    lib.pk_moe_route_noalloc.restype = ctypes.c_int
+    lib.pk_moe_route_noalloc.argtypes = [P, I32, I32, I32, P, P, P, P, P, P]
     lib.pk_moe_set_wait_limit_ns.restype = None
     lib.pk_moe_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
     lib.pk_debug_bounded_wait.restype = ctypes.c_int
@@ -148,6 +151,26 @@ def pk_moe_dispatch_gemm(x: torch.Tensor, perm: torch.Tensor, expert_offsets: to
         _ptr(out, torch.bfloat16, "out", T * k * De),
         _ptr(status_word, torch.int32, "status_word", 1), _stream(stream))
     _check(rc, "pk_moe_dispatch_gemm")
+
+
+def pk_moe_route_noalloc(topk_idx: torch.Tensor, E: int, expert_offsets: torch.Tensor,
+                         perm: torch.Tensor, expert_counts: torch.Tensor | None = None,
+                         inv_perm: torch.Tensor | None = None,
+                         status_word: torch.Tensor | None = None, stream=None) -> None:
+    """Counts, offsets, perm and inv_perm without a caller workspace: for
+    callers that cannot allocate device memory (the C call allocates none;
+    its counters live in a fixed 1 MiB array inside the library). The first
+    call on a device should come before any stream capture; calls that
+    overlap on the GPU share that array and race."""
+    T, k = topk_idx.shape
+    rc = lib.pk_moe_route_noalloc(
+        _ptr(topk_idx, torch.int32, "topk_idx"), T, k, E,
+        _ptr(expert_counts, torch.int32, "expert_counts", E),
+        _ptr(expert_offsets, torch.int32, "expert_offsets", E + 1),
+        _ptr(perm, torch.int32, "perm", T * k),
+        _ptr(inv_perm, torch.int32, "inv_perm", T * k),
+        _ptr(status_word, torch.int32, "status_word", 1), _stream(stream))
+    _check(rc, "pk_moe_route_noalloc")
 
 
 def pk_moe_set_wait_limit_ns(limit_ns: int) -> None:
