@@ -3,26 +3,40 @@
 // -- the "token-dispatch + GEMM" of "Loads and Loads of Fluffy Kittens"
 // ("Key claims", Fig. 17) on one device. What carries over from the pages is
 // their intra-SM overlap (section "Using the Right Overlapping Schedule"):
-// a producer warp moves tiles with TMA while the tensor cores stay busy.
+// producer warps move tiles while the tensor cores stay busy.
 //
-// Persistent kernel, one CTA per SM, 6 warps:
-//   warp 0     producer: per K-step of 64, TMA-loads the W_e tile [64 x BN]
-//              (four 64x64 boxes, 128-byte swizzle) and gathers the unit's
-//              routed x rows straight into 128-byte-swizzled shared memory
-//              with four-row TMA gathers (lane l fetches rows 4l..4l+3).
-//   warp 1     MMA issuer (one thread): tcgen05.mma M=128 x N=BN x K=16 per
-//              m-tile into fp32 accumulators in TMEM; commits free the stage.
-//   warps 2-5  epilogue: tcgen05.ld from TMEM, bf16 round-to-nearest-even,
-//              masked 16-byte stores of the valid rows and columns.
-// A 3-stage shared-memory ring (full/empty mbarriers) connects producer and
-// MMA; an accumulator barrier pair connects MMA and epilogue.
+// Persistent kernel, one CTA per SM, 10 warps:
+//   warps 0-3  epilogue: tcgen05.ld of the warp's TMEM lane quarter, bf16
+//              round-to-nearest-even, masked 16-byte stores of valid rows and
+//              columns.
+//   warp 4     MMA issuer (one thread) and TMEM owner: tcgen05.mma M=128 x
+//              N=bn x K=16 per m-tile into fp32 accumulators in TMEM; each
+//              commit frees a shared-memory stage or hands the unit's
+//              accumulators to the epilogue.
+//   warp 5     W producer (one thread): per K-step of 64 rows, TMA-loads the
+//              W_e tile [64 x bn] as 64x64 boxes, 128-byte swizzle (MN-major
+//              operand).
+//   warps 6-9  dispatch: gather the unit's routed x rows with 16-byte
+//              cp.async into K-major 128-byte-swizzled tiles (each warp
+//              instruction moves four whole 128-byte row segments); each
+//              thread's copies arrive on the stage's barrier when they land,
+//              and the MMA thread fences them into the async proxy after its
+//              wait, before the tensor cores read them.
+// Three 64 KiB stages (full/empty mbarriers) connect producers and MMA.
 //
-// Work unit = (expert e, n-tile of BN <= 256 columns, group of up to two
-// 128-row m-tiles). Both m-tiles of a unit share every W tile it loads, so an
-// expert with at most 256 rows streams its W_e exactly once. Units are
-// numbered expert-major (e, n, group) and dealt round-robin to the CTAs, so
-// units that share a W tile or the same gathered rows run at the same time
-// and meet in L2. Experts with no rows contribute no units.
+// Work unit = (expert e, group of m-tiles, n-tile), with a shape chosen per
+// expert so that TMEM (512 fp32 columns x 128 lanes) holds every accumulator
+// of the unit and each W tile is loaded once per unit:
+//   <= 2 m-tiles (<= 256 rows): one group, n-tiles of 256 columns;
+//   3 m-tiles (257..384 rows):  one group of three, n-tiles of 128 columns;
+//   >= 4 m-tiles:               groups of two, n-tiles of 256 columns.
+// So an expert with at most 384 rows streams W_e from memory exactly once.
+// Units are numbered expert by expert, group-major then n-tile, and dealt
+// round-robin to the CTAs: the n-tiles of one row group (which gather the same
+// rows) run side by side, and the groups of a heavy expert reuse W_e from L2
+// (its W loads are marked evict-last; single-group experts mark W
+// evict-first, as each tile is needed once). Experts with no rows add no
+// units.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -40,23 +54,30 @@ namespace dg {
 
 constexpr int BM = 128;                      // rows per m-tile (MMA M)
 constexpr int BK = 64;                       // K per stage: one 128-byte swizzle row of bf16
-constexpr int BN = 256;                      // widest n-tile (MMA N)
-constexpr int MT = 2;                        // m-tiles (accumulators) per unit
-constexpr int STAGES = 3;
 constexpr int B_BOX = 64;                    // W box: 64 columns x 64 rows
 constexpr int B_BOX_BYTES = B_BOX * BK * 2;  // 8 KiB
-constexpr int B_BYTES = BK * BN * 2;         // 32 KiB
-constexpr int A_BYTES = BM * BK * 2;         // 16 KiB
-constexpr int STAGE_BYTES = B_BYTES + MT * A_BYTES;
-constexpr int THREADS = 192;
-constexpr uint32_t TMEM_COLS = 512;          // MT accumulators of BN fp32 columns
+constexpr int A_BYTES = BM * BK * 2;         // 16 KiB per m-tile
+constexpr int STAGES = 3;
+constexpr int STAGE_BYTES = 64 * 1024;       // W tile (bn_max*128 B) + m-tiles
 constexpr int UMMA_K = 16;
+constexpr uint32_t TMEM_COLS = 512;
+
+constexpr int EPI_WARPS = 4;                 // warps 0..3
+constexpr int MMA_WARP = 4;
+constexpr int W_WARP = 5;
+constexpr int GATHER_WARP0 = 6;              // warps 6..9
+constexpr int GATHER_WARPS = 4;
+constexpr int GATHER_THREADS = GATHER_WARPS * 32;
+constexpr int THREADS = (GATHER_WARP0 + GATHER_WARPS) * 32;
+constexpr int ROWS_PER_PASS = GATHER_THREADS / 8;    // 8 threads per 128-byte row segment
+constexpr int ROWS_PER_THREAD = BM / ROWS_PER_PASS;  // per m-tile
+constexpr int MAX_MPU = 3;                   // m-tiles per unit
 
 struct Ctrl {
-    uint64_t full[STAGES];
-    uint64_t empty[STAGES];
-    uint64_t acc_full;
-    uint64_t acc_empty;
+    uint64_t full[STAGES];   // 1 arrive (W, + tx bytes) + one arrive per gather thread
+    uint64_t empty[STAGES];  // one tcgen05.commit
+    uint64_t acc_full;       // one tcgen05.commit per unit
+    uint64_t acc_empty;      // one arrive per epilogue warp
     uint64_t drain;
     uint32_t tmem_base;
     int abort;
@@ -67,24 +88,25 @@ constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + static_cast<int>(sizeof
 struct Unit {
     int e;        // expert
     int row0;     // first sorted row of the unit
-    int rows;     // valid rows (<= MT * BM)
-    int mtiles;   // ceil(rows / BM)
+    int rows;     // valid rows
+    int mpu;      // m-tiles in this unit
     int n0;       // first output column
-    int bn;       // n-tile width: a multiple of 64, <= BN
+    int bn;       // n-tile width (a multiple of 64)
+    int bn_max;   // n-tile width of this expert's units: accumulator column stride
+    bool shared_w;  // other units of this expert load the same W tiles
 };
 
-// Walks the expert-major unit numbering; u must not decrease between calls.
+// Walks the unit numbering; u must not decrease between calls.
 struct Walker {
     const int32_t* off;
-    int E, R, De, ntiles;
+    int E, R, De;
     int e;
     int64_t base;  // units of experts < e
-    int lo, rows, groups;
+    int lo, rows, groups, mpu_max, bn_max, ntiles;
     int64_t units;
 
     __device__ void init(const int32_t* o, int E_, int R_, int De_) {
         off = o; E = E_; R = R_; De = De_;
-        ntiles = (De + BN - 1) / BN;
         e = 0; base = 0;
         load();
     }
@@ -96,7 +118,13 @@ struct Walker {
         lo = a;
         rows = b - a;
         const int mt = (rows + BM - 1) / BM;
-        groups = (mt + MT - 1) / MT;
+        if (mt == 3) {
+            mpu_max = 3; bn_max = 128;
+        } else {
+            mpu_max = 2; bn_max = 256;
+        }
+        groups = (mt + mpu_max - 1) / mpu_max;
+        ntiles = (De + bn_max - 1) / bn_max;
         units = static_cast<int64_t>(groups) * ntiles;
     }
     __device__ bool find(int64_t u, Unit& U) {
@@ -107,13 +135,15 @@ struct Walker {
         }
         if (e >= E) return false;
         const int l = static_cast<int>(u - base);
-        const int n = l / groups, g = l - n * groups;
+        const int g = l / ntiles, n = l - g * ntiles;
         U.e = e;
-        U.row0 = lo + g * (MT * BM);
-        U.rows = min(MT * BM, rows - g * (MT * BM));
-        U.mtiles = (U.rows + BM - 1) / BM;
-        U.n0 = n * BN;
-        U.bn = min(BN, (De - U.n0 + B_BOX - 1) / B_BOX * B_BOX);
+        U.row0 = lo + g * (mpu_max * BM);
+        U.rows = min(mpu_max * BM, rows - g * (mpu_max * BM));
+        U.mpu = (U.rows + BM - 1) / BM;
+        U.n0 = n * bn_max;
+        U.bn = min(bn_max, (De - U.n0 + B_BOX - 1) / B_BOX * B_BOX);
+        U.bn_max = bn_max;
+        U.shared_w = groups > 1;
         return true;
     }
 };
@@ -133,8 +163,26 @@ __device__ __forceinline__ void fail(volatile int* abort, int32_t* status) {
     *abort = 1;
 }
 
+__device__ __forceinline__ void store_row_chunk(uint16_t* dst, const uint32_t (&v)[32], int col0,
+                                                int De) {
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+        if (col0 + g * 8 < De) {
+            uint4 pkd;
+            uint32_t* w = reinterpret_cast<uint32_t*>(&pkd);
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+                __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(v[g * 8 + 2 * h]),
+                                                          __uint_as_float(v[g * 8 + 2 * h + 1]));
+                w[h] = *reinterpret_cast<uint32_t*>(&b2);
+            }
+            *reinterpret_cast<uint4*>(dst + col0 + g * 8) = pkd;
+        }
+    }
+}
+
 __global__ void __launch_bounds__(THREADS, 1)
-    k_dispatch_gemm(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap wmap,
+    k_dispatch_gemm(const __grid_constant__ CUtensorMap wmap, const uint16_t* __restrict__ x,
                     const int32_t* __restrict__ perm, const int32_t* __restrict__ offsets,
                     uint16_t* __restrict__ out, int32_t T, int32_t k, int32_t D, int32_t E,
                     int32_t De, int32_t* status, uint64_t limit) {
@@ -157,20 +205,17 @@ __global__ void __launch_bounds__(THREADS, 1)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
-            mbar_init(full0 + 8 * s, 1);
+            mbar_init(full0 + 8 * s, 1 + GATHER_THREADS);
             mbar_init(empty0 + 8 * s, 1);
         }
         mbar_init(acc_full, 1);
-        mbar_init(acc_empty, 4);
+        mbar_init(acc_empty, EPI_WARPS);
         mbar_init(drain, 1);
         ctl->abort = 0;
         fence_barrier_init();
     }
-    if (warp == 0 && lane == 0) {
-        prefetch_tensormap(&xmap);
-        prefetch_tensormap(&wmap);
-    }
-    if (warp == 1) {
+    if (warp == W_WARP && lane == 0) prefetch_tensormap(&wmap);
+    if (warp == MMA_WARP) {
         tmem_alloc(smem_addr(&ctl->tmem_base), TMEM_COLS);
         tmem_relinquish();
     }
@@ -179,76 +224,108 @@ __global__ void __launch_bounds__(THREADS, 1)
     tc_fence_after_sync();
     const uint32_t tmem = ctl->tmem_base;
 
-    if (warp == 0) {
-        // ------------------------------------------------------ producer
-        const uint64_t pol_w = policy_evict_first();  // each W tile is needed once
-        const uint64_t pol_x = policy_evict_last();   // rows are re-read by other n-tiles
+    if (warp >= GATHER_WARP0) {
+        // ------------------------------------------------------ dispatch
+        const int gt = threadIdx.x - GATHER_WARP0 * 32;
+        const int c = gt & 7;          // 16-byte chunk of the 128-byte row segment
+        const int rb = gt >> 3;        // first row of this thread (0..15)
+        const uint32_t swz = static_cast<uint32_t>(((c ^ (rb & 7)) << 4));
+        const uint64_t pol_x = policy_evict_last();  // rows are re-read by the unit's other n-tiles
         Walker wk;
         wk.init(offsets, E, R, De);
         int stage = 0;
-        uint32_t phase = 0, issued = 0, issued_par = 0;
+        uint32_t phase = 0;
         bool ok = true, bad = false;
         for (int64_t u = blockIdx.x; ok; u += gridDim.x) {
             Unit U;
             if (!wk.find(u, U)) break;
-            int rr[MT][4];
-            bool go[MT];
-            uint32_t bytes = static_cast<uint32_t>(U.bn / B_BOX) * B_BOX_BYTES;
+            const char* src[MAX_MPU][ROWS_PER_THREAD];
 #pragma unroll
-            for (int mt = 0; mt < MT; ++mt) {
-                const int p0 = mt * BM + 4 * lane;
-                go[mt] = mt < U.mtiles && p0 < U.rows;
+            for (int mt = 0; mt < MAX_MPU; ++mt)
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    int t = 0;
-                    if (go[mt]) {
-                        const int p = (p0 + i < U.rows) ? p0 + i : p0;
-                        int f = __ldg(perm + U.row0 + p);
+                for (int i = 0; i < ROWS_PER_THREAD; ++i) {
+                    const int r = mt * BM + rb + ROWS_PER_PASS * i;
+                    const char* p = nullptr;
+                    if (mt < U.mpu && r < U.rows) {
+                        int f = __ldg(perm + U.row0 + r);
                         if (f < 0 || f >= R) {
                             bad = true;
                             f = 0;
                         }
-                        t = f / k;
+                        p = reinterpret_cast<const char*>(x + static_cast<int64_t>(f / k) * D) +
+                            c * 16;
                     }
-                    rr[mt][i] = t;
+                    src[mt][i] = p;
                 }
-                const int vm = min(max(U.rows - mt * BM, 0), BM);
-                bytes += static_cast<uint32_t>((vm + 3) / 4) * (4 * BK * 2);
-            }
+            const uint32_t a_off = static_cast<uint32_t>(U.bn_max) * (BK * 2);
             for (int ks = 0; ks < nk; ++ks) {
                 if (!warp_wait(empty0 + 8 * stage, phase ^ 1u, abort, limit)) {
                     if (lane == 0) fail(abort, status);
                     ok = false;
                     break;
                 }
-                const uint32_t full = full0 + 8 * stage;
-                if (lane == 0) mbar_arrive_expect_tx(full, bytes);
-                __syncwarp();
-                const uint32_t sb = sbase + stage * STAGE_BYTES;
-                if (lane < U.bn / B_BOX)
-                    tma_load_3d(sb + lane * B_BOX_BYTES, &wmap, U.n0 + lane * B_BOX, ks * BK, U.e,
-                                full, pol_w);
+                const uint32_t dst0 = sbase + stage * STAGE_BYTES + a_off + rb * 128 + swz;
+                const uint32_t nbytes = (ks * BK + c * 8 < D) ? 16u : 0u;
+                const int64_t koff = static_cast<int64_t>(ks) * BK * 2;
 #pragma unroll
-                for (int mt = 0; mt < MT; ++mt)
-                    if (go[mt])
-                        tma_gather4(sb + B_BYTES + mt * A_BYTES + lane * (4 * BK * 2), &xmap,
-                                    ks * BK, rr[mt][0], rr[mt][1], rr[mt][2], rr[mt][3], full,
-                                    pol_x);
-                issued |= 1u << stage;
-                issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
+                for (int mt = 0; mt < MAX_MPU; ++mt)
+#pragma unroll
+                    for (int i = 0; i < ROWS_PER_THREAD; ++i)
+                        if (src[mt][i])
+                            cp_async_16(dst0 + mt * A_BYTES + i * (ROWS_PER_PASS * 128),
+                                        nbytes ? src[mt][i] + koff : src[mt][i], nbytes, pol_x);
+                cp_async_arrive_noinc(full0 + 8 * stage);
                 if (++stage == STAGES) {
                     stage = 0;
                     phase ^= 1u;
                 }
             }
         }
+        // Copies still in flight must land before the CTA may exit.
+        cp_async_wait_all();
         if (bad) report(status, PK_ERR_BAD_INDEX);
-        // Every copy this warp started must land before the CTA may exit.
-        if (lane == 0)
+    } else if (warp == W_WARP) {
+        // ----------------------------------------------------- W producer
+        if (lane == 0) {
+            const uint64_t pol_once = policy_evict_first();
+            const uint64_t pol_reuse = policy_evict_last();
+            Walker wk;
+            wk.init(offsets, E, R, De);
+            int stage = 0;
+            uint32_t phase = 0, issued = 0, issued_par = 0;
+            bool ok = true;
+            for (int64_t u = blockIdx.x; ok; u += gridDim.x) {
+                Unit U;
+                if (!wk.find(u, U)) break;
+                const int nbox = U.bn / B_BOX;
+                const uint64_t pol = U.shared_w ? pol_reuse : pol_once;
+                for (int ks = 0; ks < nk; ++ks) {
+                    if (!mbar_wait(empty0 + 8 * stage, phase ^ 1u, abort, limit)) {
+                        fail(abort, status);
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t full = full0 + 8 * stage;
+                    mbar_arrive_expect_tx(full, static_cast<uint32_t>(nbox) * B_BOX_BYTES);
+                    const uint32_t sb = sbase + stage * STAGE_BYTES;
+                    for (int b = 0; b < nbox; ++b)
+                        tma_load_3d(sb + b * B_BOX_BYTES, &wmap, U.n0 + b * B_BOX, ks * BK, U.e,
+                                    full, pol);
+                    issued |= 1u << stage;
+                    issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            // Every copy this thread started must land before the CTA may exit.
             for (int s = 0; s < STAGES; ++s)
-                if ((issued >> s) & 1u) mbar_wait(full0 + 8 * s, (issued_par >> s) & 1u, nullptr, limit);
+                if ((issued >> s) & 1u)
+                    mbar_wait(full0 + 8 * s, (issued_par >> s) & 1u, nullptr, limit);
+        }
         __syncwarp();
-    } else if (warp == 1) {
+    } else if (warp == MMA_WARP) {
         // ----------------------------------------------------------- MMA
         if (lane == 0) {
             Walker wk;
@@ -265,6 +342,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
                 tc_fence_after_sync();
                 const uint32_t idesc = idesc_bf16_f32(BM, U.bn, true);
+                const uint32_t a_off = static_cast<uint32_t>(U.bn_max) * (BK * 2);
                 for (int ks = 0; ks < nk; ++ks) {
                     if (!mbar_wait(full0 + 8 * stage, phase, abort, limit)) {
                         fail(abort, status);
@@ -272,19 +350,23 @@ __global__ void __launch_bounds__(THREADS, 1)
                         break;
                     }
                     tc_fence_after_sync();
+                    // The gathered rows were written by cp.async (generic proxy);
+                    // order them before the tensor cores' async-proxy reads.
+                    fence_proxy_async_smem();
                     const uint32_t sb = sbase + stage * STAGE_BYTES;
-                    for (int mt = 0; mt < U.mtiles; ++mt) {
+                    for (int mt = 0; mt < U.mpu; ++mt) {
 #pragma unroll
                         for (int kk = 0; kk < BK / UMMA_K; ++kk) {
                             // A: K-major, rows 128 B apart, 8-row groups 1024 B apart;
                             // a K step of 16 moves 32 B inside the swizzled row.
                             const uint64_t a = sdesc_sw128(
-                                sb + B_BYTES + mt * A_BYTES + kk * (UMMA_K * 2), 16, 1024);
+                                sb + a_off + mt * A_BYTES + kk * (UMMA_K * 2), 16, 1024);
                             // B: MN-major (W rows are N-contiguous), 64-column blocks
                             // 8 KiB apart (LBO), 8-row K groups 1024 B apart (SBO);
                             // a K step of 16 moves 16 rows = 2 KiB.
-                            const uint64_t b = sdesc_sw128(sb + kk * (UMMA_K * 128), B_BOX_BYTES, 1024);
-                            mma_bf16(tmem + static_cast<uint32_t>(mt * BN), a, b, idesc,
+                            const uint64_t b =
+                                sdesc_sw128(sb + kk * (UMMA_K * 128), B_BOX_BYTES, 1024);
+                            mma_bf16(tmem + static_cast<uint32_t>(mt * U.bn_max), a, b, idesc,
                                      (ks | kk) != 0 ? 1u : 0u);
                         }
                     }
@@ -305,7 +387,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         __syncwarp();
     } else {
         // ------------------------------------------------------ epilogue
-        const int q = warp & 3;  // TMEM lane quarter this warp may access
+        const int q = warp;  // TMEM lane quarter this warp may access (warps 0..3)
         Walker wk;
         wk.init(offsets, E, R, De);
         uint32_t acc_phase = 0;
@@ -317,48 +399,49 @@ __global__ void __launch_bounds__(THREADS, 1)
                 break;
             }
             tc_fence_after_sync();
-            for (int mt = 0; mt < U.mtiles; ++mt) {
+            // Last m-tile with rows in this warp's quarter: TMEM is released
+            // after its last load, before its last stores.
+            int last_mt = -1;
+            for (int mt = 0; mt < U.mpu; ++mt)
+                if (mt * BM + q * 32 < U.rows) last_mt = mt;
+            bool released = false;
+            for (int mt = 0; mt <= last_mt; ++mt) {
                 const int rbase = mt * BM + q * 32;
                 if (rbase >= U.rows) continue;  // warp-uniform
                 const int r = rbase + lane;
                 const bool valid = r < U.rows;
                 uint16_t* orow = out + static_cast<int64_t>(U.row0 + r) * De;
                 const uint32_t tbase = tmem + (static_cast<uint32_t>(q * 32) << 16) +
-                                       static_cast<uint32_t>(mt * BN);
-                for (int c = 0; c < U.bn / 32; ++c) {
-                    uint32_t v[32];
-                    tmem_ld_32x32b_x32(tbase + c * 32, v);
+                                       static_cast<uint32_t>(mt * U.bn_max);
+                for (int cc = 0; cc < U.bn / 32; cc += 2) {
+                    uint32_t v0[32], v1[32];
+                    tmem_ld_32x32b_x32(tbase + cc * 32, v0);
+                    tmem_ld_32x32b_x32(tbase + cc * 32 + 32, v1);
                     tmem_wait_ld();
-                    const int col0 = U.n0 + c * 32;
+                    if (mt == last_mt && cc + 2 >= U.bn / 32) {
+                        tc_fence_before_sync();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(acc_empty);
+                        released = true;
+                    }
                     if (valid) {
-#pragma unroll
-                        for (int g = 0; g < 4; ++g) {
-                            if (col0 + g * 8 < De) {
-                                uint4 pkd;
-                                uint32_t* w = reinterpret_cast<uint32_t*>(&pkd);
-#pragma unroll
-                                for (int h = 0; h < 4; ++h) {
-                                    __nv_bfloat162 b2 = __floats2bfloat162_rn(
-                                        __uint_as_float(v[g * 8 + 2 * h]),
-                                        __uint_as_float(v[g * 8 + 2 * h + 1]));
-                                    w[h] = *reinterpret_cast<uint32_t*>(&b2);
-                                }
-                                *reinterpret_cast<uint4*>(orow + col0 + g * 8) = pkd;
-                            }
-                        }
+                        store_row_chunk(orow, v0, U.n0 + cc * 32, De);
+                        store_row_chunk(orow, v1, U.n0 + cc * 32 + 32, De);
                     }
                 }
             }
-            tc_fence_before_sync();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(acc_empty);
+            if (!released) {
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(acc_empty);
+            }
             acc_phase ^= 1u;
         }
     }
 
     tc_fence_before_sync();
     __syncthreads();
-    if (warp == 1) {
+    if (warp == MMA_WARP) {
         tc_fence_after_sync();
         tmem_dealloc(tmem, TMEM_COLS);
     }
@@ -417,17 +500,7 @@ int launch_dispatch_gemm(const uint16_t* x, const int32_t* perm, const int32_t* 
         sms = di.sms;
     }
 
-    CUtensorMap xmap, wmap;
-    {
-        cuuint64_t dims[2] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(T)};
-        cuuint64_t strides[1] = {static_cast<cuuint64_t>(D) * 2};
-        cuuint32_t box[2] = {BK, 1};
-        cuuint32_t es[2] = {1, 1};
-        if (enc(&xmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(x), dims, strides,
-                box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-            return PK_ERR_UNSUPPORTED;
-    }
+    CUtensorMap wmap;
     {
         cuuint64_t dims[3] = {static_cast<cuuint64_t>(De), static_cast<cuuint64_t>(D),
                               static_cast<cuuint64_t>(E)};
@@ -440,8 +513,8 @@ int launch_dispatch_gemm(const uint16_t* x, const int32_t* perm, const int32_t* 
                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return PK_ERR_UNSUPPORTED;
     }
-    k_dispatch_gemm<<<sms, THREADS, SMEM_BYTES, stream>>>(xmap, wmap, perm, offsets, out, T, k, D,
-                                                         E, De, status, wait_limit_ns);
+    k_dispatch_gemm<<<sms, THREADS, SMEM_BYTES, stream>>>(wmap, x, perm, offsets, out, T, k, D, E,
+                                                         De, status, wait_limit_ns);
     return cudaGetLastError() == cudaSuccess ? PK_OK : PK_ERR_CUDA;
 }
 
