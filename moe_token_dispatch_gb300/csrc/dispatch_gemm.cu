@@ -5,7 +5,7 @@
 // their intra-SM overlap (section "Using the Right Overlapping Schedule"):
 // producer warps move tiles while the tensor cores stay busy.
 //
-// Persistent kernel, one CTA per SM, 10 warps:
+// Persistent kernel, one CTA per SM, 11 warps:
 //   warps 0-3  epilogue: tcgen05.ld of the warp's TMEM lane quarter, bf16
 //              round-to-nearest-even, masked 16-byte stores of valid rows and
 //              columns.
@@ -15,13 +15,18 @@
 //              accumulators to the epilogue.
 //   warp 5     W producer (one thread): per K-step of 64 rows, TMA-loads the
 //              W_e tile [64 x bn] as 64x64 boxes, 128-byte swizzle (MN-major
-//              operand).
-//   warps 6-9  dispatch: gather the unit's routed x rows with 16-byte
+//              operand), and asks TMA to prefetch into L2 the W boxes of the
+//              K-step W_PREFETCH steps ahead, so HBM latency is covered by L2
+//              rather than by shared-memory stages.
+//   warps 6,7,9,10  dispatch: gather the unit's routed x rows with 16-byte
 //              cp.async into K-major 128-byte-swizzled tiles (each warp
 //              instruction moves four whole 128-byte row segments); each
 //              thread's copies arrive on the stage's barrier when they land,
 //              and the MMA thread fences them into the async proxy after its
 //              wait, before the tensor cores read them.
+// Warp 8 only waits at the final barrier: warps share an SM sub-partition
+// with the warps whose index is equal mod 4, and this keeps the busy gather
+// warps off the MMA issuer's sub-partition.
 // Three 64 KiB stages (full/empty mbarriers) connect producers and MMA.
 //
 // Work unit = (expert e, group of m-tiles, n-tile), with a shape chosen per
@@ -65,13 +70,20 @@ constexpr uint32_t TMEM_COLS = 512;
 constexpr int EPI_WARPS = 4;                 // warps 0..3
 constexpr int MMA_WARP = 4;
 constexpr int W_WARP = 5;
-constexpr int GATHER_WARP0 = 6;              // warps 6..9
-constexpr int GATHER_WARPS = 4;
+constexpr int GATHER_WARPS = 4;              // warps 6, 7, 9, 10 (warp 8 idles)
 constexpr int GATHER_THREADS = GATHER_WARPS * 32;
-constexpr int THREADS = (GATHER_WARP0 + GATHER_WARPS) * 32;
+constexpr int THREADS = 11 * 32;
+
+// Gather-thread index 0..127 of a thread in warps 6, 7, 9, 10; -1 otherwise.
+__device__ __forceinline__ int gather_index(int warp, int lane) {
+    if (warp == 6 || warp == 7) return (warp - 6) * 32 + lane;
+    if (warp == 9 || warp == 10) return (warp - 7) * 32 + lane;
+    return -1;
+}
 constexpr int ROWS_PER_PASS = GATHER_THREADS / 8;    // 8 threads per 128-byte row segment
 constexpr int ROWS_PER_THREAD = BM / ROWS_PER_PASS;  // per m-tile
 constexpr int MAX_MPU = 3;                   // m-tiles per unit
+constexpr int W_PREFETCH = 6;                // K-steps of W prefetched into L2 ahead of the loads
 
 struct Ctrl {
     uint64_t full[STAGES];   // 1 arrive (W, + tx bytes) + one arrive per gather thread
@@ -224,9 +236,9 @@ __global__ void __launch_bounds__(THREADS, 1)
     tc_fence_after_sync();
     const uint32_t tmem = ctl->tmem_base;
 
-    if (warp >= GATHER_WARP0) {
+    const int gt = gather_index(warp, lane);
+    if (gt >= 0) {
         // ------------------------------------------------------ dispatch
-        const int gt = threadIdx.x - GATHER_WARP0 * 32;
         const int c = gt & 7;          // 16-byte chunk of the 128-byte row segment
         const int rb = gt >> 3;        // first row of this thread (0..15)
         const uint32_t swz = static_cast<uint32_t>(((c ^ (rb & 7)) << 4));
@@ -289,8 +301,25 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (lane == 0) {
             const uint64_t pol_once = policy_evict_first();
             const uint64_t pol_reuse = policy_evict_last();
-            Walker wk;
+            Walker wk, pf;
             wk.init(offsets, E, R, De);
+            pf.init(offsets, E, R, De);
+            // Prefetch cursor: unit pf_u, K-step pf_ks, W_PREFETCH steps ahead.
+            int64_t pf_u = blockIdx.x;
+            int pf_ks = 0;
+            Unit PU;
+            bool pf_live = pf.find(pf_u, PU);
+            auto prefetch_one = [&]() {
+                if (!pf_live) return;
+                for (int b = 0; b < PU.bn / B_BOX; ++b)
+                    tma_prefetch_3d(&wmap, PU.n0 + b * B_BOX, pf_ks * BK, PU.e);
+                if (++pf_ks == nk) {
+                    pf_ks = 0;
+                    pf_u += gridDim.x;
+                    pf_live = pf.find(pf_u, PU);
+                }
+            };
+            for (int i = 0; i < W_PREFETCH; ++i) prefetch_one();
             int stage = 0;
             uint32_t phase = 0, issued = 0, issued_par = 0;
             bool ok = true;
@@ -300,6 +329,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 const int nbox = U.bn / B_BOX;
                 const uint64_t pol = U.shared_w ? pol_reuse : pol_once;
                 for (int ks = 0; ks < nk; ++ks) {
+                    prefetch_one();
                     if (!mbar_wait(empty0 + 8 * stage, phase ^ 1u, abort, limit)) {
                         fail(abort, status);
                         ok = false;
@@ -342,7 +372,17 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
                 tc_fence_after_sync();
                 const uint32_t idesc = idesc_bf16_f32(BM, U.bn, true);
-                const uint32_t a_off = static_cast<uint32_t>(U.bn_max) * (BK * 2);
+                // Descriptors of stage 0; a stage adds STAGE_BYTES, an m-tile
+                // A_BYTES, a K step of 16 adds 32 B (A, inside the swizzled
+                // row) or 16 rows = 2 KiB (B). The address field holds bytes >> 4.
+                // A: K-major, rows 128 B apart, 8-row groups 1024 B apart.
+                // B: MN-major (W rows are N-contiguous), 64-column blocks
+                // 8 KiB apart (LBO), 8-row K groups 1024 B apart (SBO).
+                const uint64_t a_desc0 =
+                    sdesc_sw128(sbase + static_cast<uint32_t>(U.bn_max) * (BK * 2), 16, 1024);
+                const uint64_t b_desc0 = sdesc_sw128(sbase, B_BOX_BYTES, 1024);
+                const int mpu = U.mpu;
+                const uint32_t acc_stride = static_cast<uint32_t>(U.bn_max);
                 for (int ks = 0; ks < nk; ++ks) {
                     if (!mbar_wait(full0 + 8 * stage, phase, abort, limit)) {
                         fail(abort, status);
@@ -353,22 +393,16 @@ __global__ void __launch_bounds__(THREADS, 1)
                     // The gathered rows were written by cp.async (generic proxy);
                     // order them before the tensor cores' async-proxy reads.
                     fence_proxy_async_smem();
-                    const uint32_t sb = sbase + stage * STAGE_BYTES;
-                    for (int mt = 0; mt < U.mpu; ++mt) {
+                    const uint64_t sdelta = static_cast<uint64_t>(stage) * (STAGE_BYTES >> 4);
+                    const uint64_t a_st = a_desc0 + sdelta, b_st = b_desc0 + sdelta;
+                    for (int mt = 0; mt < mpu; ++mt) {
+                        const uint64_t a_mt = a_st + static_cast<uint64_t>(mt) * (A_BYTES >> 4);
+                        const uint32_t d = tmem + static_cast<uint32_t>(mt) * acc_stride;
 #pragma unroll
-                        for (int kk = 0; kk < BK / UMMA_K; ++kk) {
-                            // A: K-major, rows 128 B apart, 8-row groups 1024 B apart;
-                            // a K step of 16 moves 32 B inside the swizzled row.
-                            const uint64_t a = sdesc_sw128(
-                                sb + a_off + mt * A_BYTES + kk * (UMMA_K * 2), 16, 1024);
-                            // B: MN-major (W rows are N-contiguous), 64-column blocks
-                            // 8 KiB apart (LBO), 8-row K groups 1024 B apart (SBO);
-                            // a K step of 16 moves 16 rows = 2 KiB.
-                            const uint64_t b =
-                                sdesc_sw128(sb + kk * (UMMA_K * 128), B_BOX_BYTES, 1024);
-                            mma_bf16(tmem + static_cast<uint32_t>(mt * U.bn_max), a, b, idesc,
+                        for (int kk = 0; kk < BK / UMMA_K; ++kk)
+                            mma_bf16(d, a_mt + kk * ((UMMA_K * 2) >> 4),
+                                     b_st + kk * ((UMMA_K * 128) >> 4), idesc,
                                      (ks | kk) != 0 ? 1u : 0u);
-                        }
                     }
                     mma_commit(empty0 + 8 * stage);
                     if (++stage == STAGES) {
@@ -385,7 +419,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             mbar_wait(drain, 0, nullptr, limit);
         }
         __syncwarp();
-    } else {
+    } else if (warp < EPI_WARPS) {
         // ------------------------------------------------------ epilogue
         const int q = warp;  // TMEM lane quarter this warp may access (warps 0..3)
         Walker wk;
@@ -439,6 +473,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
     }
 
+    // (warp 8 has no role and comes straight here)
     tc_fence_before_sync();
     __syncthreads();
     if (warp == MMA_WARP) {
