@@ -56,8 +56,9 @@ def source_digest(path=GEMM_SOURCE) -> str:
 
 # Workloads too large for a full ncu capture take the DRAM traffic of a smaller
 # case with the same rows per expert and tile shapes, scaled by the units of
-# work processed (experts touched): "ep" = 8 x "ep32".
-TRAFFIC_SCALED_FROM = {"ep": ("ep32", 256 / 32)}
+# work processed (experts touched): "ep" = 8 x "ep32"; "decode" touches 252 of
+# its 256 experts, "decode32" all 32 of its experts.
+TRAFFIC_SCALED_FROM = {"ep": ("ep32", 256 / 32), "decode": ("decode32", 252 / 32)}
 
 
 def profiled_traffic(workload: str):

@@ -159,6 +159,10 @@ WORKLOADS = {
     # W (0.94 GB) still exceeds L2
     "ep32": Workload("ep32", 1024, 7168, 32, 8, 2048,
                      desc="ep shape with 32 experts and 1024 tokens (profiling size)"),
+    # profiling case for the decode workload: ~4 rows per expert as in
+    # "decode", 32 experts so that W (0.94 GB) still exceeds L2
+    "decode32": Workload("decode32", 16, 7168, 32, 8, 2048,
+                         desc="decode shape with 32 experts and 16 tokens (profiling size)"),
 }
 
 
