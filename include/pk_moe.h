@@ -131,6 +131,39 @@ int pk_moe_dispatch_gemm(const uint16_t* x, const int32_t* perm, const int32_t* 
                          int32_t D_expert, uint16_t* out, int32_t* status_word, void* stream);
 
 /*
+ * Router top-k (the selection the expert-parallel workload of "Key claims",
+ * Fig. 17 describes with top_k=8 of num_experts=256; the pages leave the
+ * router itself open): for every token t,
+ *   topk_idx[t, s] = expert with the s-th largest logits[t, :] (equal logits
+ *                    go to the lower expert index, so the k experts differ)
+ *   gates[t, s]    = exp(l_s - l_0) / sum_s' exp(l_s' - l_0), l_s the
+ *                    selected logits (softmax over the k selected)
+ *   logits    device fp32 [T, E], read only (NaN logits are not supported)
+ *   topk_idx  device int32 [T, k], written
+ *   gates     device fp32 [T, k], written; may be NULL
+ * Requires T >= 0, 1 <= k <= min(E, 32), E <= PK_ROUTER_MAX_EXPERTS.
+ */
+#define PK_ROUTER_MAX_EXPERTS 1024
+int pk_moe_router_topk(const float* logits, int32_t T, int32_t E, int32_t k, int32_t* topk_idx,
+                       float* gates, void* stream);
+
+/*
+ * Combine: un-permute the expert outputs back to token order and weight them
+ * (the step after the expert MLP in the expert-parallel token-dispatch +
+ * GEMM, "Key claims", Fig. 17; the pages leave the gating open):
+ *   y[t, c] = bf16_rne( sum_{s=0..k-1} gates[t, s] * src[inv_perm[t*k + s], c] )
+ * with fp32 products and sum, s ascending.
+ *   src       device bf16 [T*k, C] in expert-sorted row order, 16-byte aligned
+ *   inv_perm  device int32 [T*k] from pk_moe_build_perm
+ *   gates     device fp32 [T, k]; NULL means every gate is 1
+ *   y         device bf16 [T, C], 16-byte aligned, written
+ * Requires C a multiple of 8, T*k < 2^31. An inv_perm entry outside
+ * [0, T*k) sets PK_ERR_BAD_INDEX and row 0 is read in its place.
+ */
+int pk_moe_combine(const uint16_t* src, const int32_t* inv_perm, const float* gates, int32_t T,
+                   int32_t k, int32_t C, uint16_t* y, int32_t* status_word, void* stream);
+
+/*
  * Routing without any device allocation (the pages have no counterpart: this
  * is an interface convenience, not a step of the method). Computes exactly
  * what pk_moe_route_counts followed by pk_moe_build_perm compute (counts,

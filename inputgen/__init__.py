@@ -32,6 +32,8 @@ _LIB = os.path.join(_HERE, "libinputgen.so")
 STREAM_X = 1
 STREAM_W = 2
 STREAM_LOGITS = 3
+STREAM_GATES = 4
+STREAM_SRC = 5
 
 
 def build(force: bool = False) -> str:
@@ -68,6 +70,12 @@ def _L():
         lib.ig_topk_routing.argtypes = [ctypes.c_uint64, ctypes.c_uint64, ctypes.c_int64,
                                         ctypes.c_int64, ctypes.c_int64, ctypes.c_double,
                                         ctypes.c_void_p, ctypes.c_int]
+        lib.ig_logits_f32.restype = ctypes.c_int
+        lib.ig_logits_f32.argtypes = [ctypes.c_uint64, ctypes.c_uint64, ctypes.c_int64,
+                                      ctypes.c_int64, ctypes.c_double, ctypes.c_void_p]
+        lib.ig_weights_f32.restype = ctypes.c_int
+        lib.ig_weights_f32.argtypes = [ctypes.c_uint64, ctypes.c_uint64, ctypes.c_int64,
+                                       ctypes.c_int64, ctypes.c_void_p]
         _lib = lib
     return _lib
 
@@ -209,6 +217,27 @@ def make_W(wl: Workload, threads=None, experts=None) -> np.ndarray:
 
 def make_topk(wl: Workload, threads=None) -> np.ndarray:
     return topk_routing(wl.seed, wl.T, wl.E, wl.k, wl.zipf_s, threads)
+
+
+def make_logits(wl: Workload) -> np.ndarray:
+    """float32 [T, E] router logits (N(0,1), plus the Zipf bias when set)."""
+    out = np.empty((wl.T, wl.E), dtype=np.float32)
+    if wl.T:
+        _L().ig_logits_f32(wl.seed, STREAM_LOGITS, wl.T, wl.E, float(wl.zipf_s), out.ctypes.data)
+    return out
+
+
+def make_gates(wl: Workload) -> np.ndarray:
+    """float32 [T, k] positive weights summing to one per token (combine input)."""
+    out = np.empty((wl.T, wl.k), dtype=np.float32)
+    if wl.T:
+        _L().ig_weights_f32(wl.seed, STREAM_GATES, wl.T, wl.k, out.ctypes.data)
+    return out
+
+
+def make_src(wl: Workload, C: int, threads=None) -> np.ndarray:
+    """bf16 bits [T*k, C] ~ N(0,1): expert outputs in sorted row order (combine input)."""
+    return normal_bf16(wl.seed, STREAM_SRC, 0, wl.R * C, 1.0, threads=threads).reshape(wl.R, C)
 
 
 def make_case(wl: Workload | str, with_W: bool = True, threads=None) -> Case:

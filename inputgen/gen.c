@@ -179,3 +179,31 @@ int ig_topk_routing(uint64_t seed, uint64_t stream, int64_t T, int64_t E, int64_
     free(taken);
     return 0;
 }
+
+/* ---- router logits and combine gates ----------------------------------- */
+/* logits[t][e] = float32(N(0,1)[t*E + e] - zipf_s * ln(e + 1)), the same
+ * stream and bias as the routing above (rounded to float32). */
+int ig_logits_f32(uint64_t seed, uint64_t stream, int64_t T, int64_t E, double zipf_s,
+                  float* out) {
+    const uint64_t key = ig_stream_key(seed, stream);
+    for (int64_t t = 0; t < T; ++t)
+        for (int64_t e = 0; e < E; ++e) {
+            double v = ig_normal_at(key, (uint64_t)(t * E + e));
+            if (zipf_s > 0.0) v -= zipf_s * log((double)(e + 1));
+            out[t * E + e] = (float)v;
+        }
+    return 0;
+}
+
+/* Positive weights that sum to one per token: u[t][s] uniform in (0, 1],
+ * divided by the token's sum, rounded to float32. */
+int ig_weights_f32(uint64_t seed, uint64_t stream, int64_t T, int64_t k, float* out) {
+    const uint64_t key = ig_stream_key(seed, stream);
+    for (int64_t t = 0; t < T; ++t) {
+        double sum = 0.0;
+        for (int64_t s = 0; s < k; ++s) sum += u01(key, (uint64_t)(t * k + s));
+        for (int64_t s = 0; s < k; ++s)
+            out[t * k + s] = (float)(u01(key, (uint64_t)(t * k + s)) / sum);
+    }
+    return 0;
+}

@@ -17,14 +17,17 @@ from ._binding import (  # noqa: F401
     PK_MAX_EXPERTS,
     PK_NOALLOC_SCRATCH_BYTES,
     PK_OK,
+    PK_ROUTER_MAX_EXPERTS,
     PkError,
     lib,
     pk_abi_version,
     pk_debug_bounded_wait,
     pk_moe_build_perm,
+    pk_moe_combine,
     pk_moe_dispatch_gemm,
     pk_moe_route_counts,
     pk_moe_route_noalloc,
+    pk_moe_router_topk,
     pk_moe_set_wait_limit_ns,
     pk_moe_workspace_bytes,
     pk_status_str,

@@ -22,6 +22,7 @@ PK_ERR_TIMEOUT = 4
 PK_ERR_BAD_INDEX = 5
 PK_MAX_EXPERTS = 4096
 PK_NOALLOC_SCRATCH_BYTES = 1 << 20
+PK_ROUTER_MAX_EXPERTS = 1024
 
 
 class PkError(RuntimeError):
@@ -50,6 +51,10 @@ def _load():
     lib.pk_moe_dispatch_gemm.argtypes = [P, P, P, P, I32, I32, I32, I32, I32, P, P, P]
     lib.pk_moe_route_noalloc.restype = ctypes.c_int
     lib.pk_moe_route_noalloc.argtypes = [P, I32, I32, I32, P, P, P, P, P, P]
+    lib.pk_moe_router_topk.restype = ctypes.c_int
+    lib.pk_moe_router_topk.argtypes = [P, I32, I32, I32, P, P, P]
+    lib.pk_moe_combine.restype = ctypes.c_int
+    lib.pk_moe_combine.argtypes = [P, P, P, I32, I32, I32, P, P, P]
     lib.pk_moe_set_wait_limit_ns.restype = None
     lib.pk_moe_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
     lib.pk_debug_bounded_wait.restype = ctypes.c_int
@@ -151,6 +156,29 @@ def pk_moe_dispatch_gemm(x: torch.Tensor, perm: torch.Tensor, expert_offsets: to
         _ptr(out, torch.bfloat16, "out", T * k * De),
         _ptr(status_word, torch.int32, "status_word", 1), _stream(stream))
     _check(rc, "pk_moe_dispatch_gemm")
+
+
+def pk_moe_router_topk(logits: torch.Tensor, k: int, topk_idx: torch.Tensor,
+                       gates: torch.Tensor | None = None, stream=None) -> None:
+    T, E = logits.shape
+    rc = lib.pk_moe_router_topk(_ptr(logits, torch.float32, "logits"), T, E, k,
+                                _ptr(topk_idx, torch.int32, "topk_idx", T * k),
+                                _ptr(gates, torch.float32, "gates", T * k), _stream(stream))
+    _check(rc, "pk_moe_router_topk")
+
+
+def pk_moe_combine(src: torch.Tensor, inv_perm: torch.Tensor, gates: torch.Tensor | None,
+                   T: int, k: int, y: torch.Tensor, status_word: torch.Tensor | None = None,
+                   stream=None) -> None:
+    R, C = src.shape
+    if R < T * k:
+        raise ValueError(f"src has {R} rows, needs T*k = {T * k}")
+    rc = lib.pk_moe_combine(_ptr(src, torch.bfloat16, "src"),
+                            _ptr(inv_perm, torch.int32, "inv_perm", T * k),
+                            _ptr(gates, torch.float32, "gates", T * k), T, k, C,
+                            _ptr(y, torch.bfloat16, "y", T * C),
+                            _ptr(status_word, torch.int32, "status_word", 1), _stream(stream))
+    _check(rc, "pk_moe_combine")
 
 
 def pk_moe_route_noalloc(topk_idx: torch.Tensor, E: int, expert_offsets: torch.Tensor,

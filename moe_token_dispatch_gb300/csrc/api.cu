@@ -89,6 +89,30 @@ int pk_moe_dispatch_gemm(const uint16_t* x, const int32_t* perm, const int32_t* 
                                     g_wait_limit_ns.load(std::memory_order_relaxed));
 }
 
+int pk_moe_router_topk(const float* logits, int32_t T, int32_t E, int32_t k, int32_t* topk_idx,
+                       float* gates, void* stream) {
+    if (T < 0 || E < 1 || k < 1 || k > E || k > 32) return PK_ERR_INVALID_ARG;
+    if (E > PK_ROUTER_MAX_EXPERTS) return PK_ERR_UNSUPPORTED;
+    if (T > 0 && (!logits || !topk_idx)) return PK_ERR_INVALID_ARG;
+    if (static_cast<int64_t>(T) * E >= (int64_t{1} << 40)) return PK_ERR_UNSUPPORTED;
+    cudaError_t err = pk::launch_router_topk(logits, T, E, k, topk_idx, gates,
+                                             static_cast<cudaStream_t>(stream));
+    return err == cudaSuccess ? PK_OK : PK_ERR_CUDA;
+}
+
+int pk_moe_combine(const uint16_t* src, const int32_t* inv_perm, const float* gates, int32_t T,
+                   int32_t k, int32_t C, uint16_t* y, int32_t* status_word, void* stream) {
+    if (T < 0 || k < 1 || C < 1 || (C % 8) != 0) return PK_ERR_INVALID_ARG;
+    const int64_t R = static_cast<int64_t>(T) * k;
+    if (R >= (int64_t{1} << 31)) return PK_ERR_UNSUPPORTED;
+    if (T == 0) return PK_OK;
+    if (!src || !inv_perm || !y) return PK_ERR_INVALID_ARG;
+    if (!aligned16(src) || !aligned16(y)) return PK_ERR_INVALID_ARG;
+    cudaError_t err = pk::launch_combine(src, inv_perm, gates, T, k, C, y, status_word,
+                                         static_cast<cudaStream_t>(stream));
+    return err == cudaSuccess ? PK_OK : PK_ERR_CUDA;
+}
+
 void pk_moe_set_wait_limit_ns(uint64_t limit_ns) {
     g_wait_limit_ns.store(limit_ns ? limit_ns : kDefaultWaitLimitNs, std::memory_order_relaxed);
 }

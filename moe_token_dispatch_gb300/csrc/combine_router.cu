@@ -1,0 +1,193 @@
+// The steps on either side of the dispatch + expert GEMM of "Loads and Loads
+// of Fluffy Kittens" ("Key claims", Fig. 17: top_k=8, num_experts=256):
+//
+//   k_router_topk  the router's selection: for every token, the k experts
+//                  with the largest logits (largest first, equal logits to
+//                  the lower expert) and gates = softmax over those k logits.
+//   k_combine      un-permute and weight the expert outputs back into token
+//                  order: y[t, :] = sum_s gates[t, s] * src[inv_perm[t*k+s], :],
+//                  fp32 accumulation in increasing s, one bf16 rounding.
+//
+// Both are memory-bound streaming kernels: one warp per token (router) or per
+// (token, 256-column chunk) (combine), 16-byte vector loads, grids sized to a
+// few resident warps per SM sub-partition.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "pk_internal.h"
+#include "pk_ptx.cuh"
+
+namespace pk {
+
+// ------------------------------------------------------------------ router
+constexpr int kRouterMaxPerLane = PK_ROUTER_MAX_EXPERTS / 32;
+
+__global__ void __launch_bounds__(256)
+    k_router_topk(const float* __restrict__ logits, int32_t T, int32_t E, int32_t k,
+                  int32_t* __restrict__ topk, float* __restrict__ gates) {
+    const int lane = threadIdx.x & 31;
+    const int64_t warp0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+    const int per = (E + 31) / 32;
+    for (int64_t t = warp0; t < T; t += nwarps) {
+        const float* row = logits + t * E;
+        float v[kRouterMaxPerLane];
+#pragma unroll
+        for (int i = 0; i < kRouterMaxPerLane; ++i) {
+            const int e = i * 32 + lane;
+            v[i] = (i < per && e < E) ? __ldg(row + e) : -INFINITY;
+        }
+        uint32_t taken = 0;
+        float my_val = -INFINITY;
+        int my_idx = 0;
+        for (int s = 0; s < k; ++s) {
+            // this lane's best untaken entry; e grows with i, so replacing only
+            // on a strictly larger value keeps the lowest index among equals
+            constexpr int kNone = 0x7fffffff;
+            float bv = -INFINITY;
+            int bi = kNone;
+#pragma unroll
+            for (int i = 0; i < kRouterMaxPerLane; ++i) {
+                const int e = i * 32 + lane;
+                if (i < per && e < E && !((taken >> i) & 1u) && (bi == kNone || v[i] > bv)) {
+                    bv = v[i];
+                    bi = e;
+                }
+            }
+            for (int d = 16; d > 0; d >>= 1) {
+                const float ov = __shfl_xor_sync(0xffffffffu, bv, d);
+                const int oi = __shfl_xor_sync(0xffffffffu, bi, d);
+                if (oi != kNone && (bi == kNone || ov > bv || (ov == bv && oi < bi))) {
+                    bv = ov;
+                    bi = oi;
+                }
+            }
+            if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+            if (lane == s) {
+                my_val = bv;
+                my_idx = bi;
+            }
+        }
+        // softmax over the selected logits, shifted by the largest (slot 0)
+        const float m = __shfl_sync(0xffffffffu, my_val, 0);
+        const float ex = lane < k ? expf(my_val - m) : 0.0f;
+        float z = ex;
+        for (int d = 16; d > 0; d >>= 1) z += __shfl_xor_sync(0xffffffffu, z, d);
+        if (lane < k) {
+            topk[t * k + lane] = my_idx;
+            if (gates) gates[t * k + lane] = ex / z;
+        }
+    }
+}
+
+// ----------------------------------------------------------------- combine
+constexpr int kCombineSlotBatch = 8;  // source rows loaded before they are summed
+
+__device__ __forceinline__ uint4 ld_nc_v4(const void* p) {
+    uint4 r;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p));
+    return r;
+}
+
+__global__ void __launch_bounds__(256)
+    k_combine(const uint16_t* __restrict__ src, const int32_t* __restrict__ inv_perm,
+              const float* __restrict__ gates, int32_t T, int32_t k, int32_t C,
+              uint16_t* __restrict__ y, int32_t* status) {
+    const int lane = threadIdx.x & 31;
+    const int64_t warp0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+    const int chunks = (C + 255) / 256;
+    const int64_t items = static_cast<int64_t>(T) * chunks;
+    const int64_t R = static_cast<int64_t>(T) * k;
+    bool bad = false;
+    for (int64_t it = warp0; it < items; it += nwarps) {
+        const int64_t t = it / chunks;
+        const int c0 = static_cast<int>(it - t * chunks) * 256 + lane * 8;
+        const bool active = c0 < C;
+        float acc[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+        for (int s0 = 0; s0 < k; s0 += kCombineSlotBatch) {
+            uint4 v[kCombineSlotBatch];
+            float g[kCombineSlotBatch];
+#pragma unroll
+            for (int i = 0; i < kCombineSlotBatch; ++i) {
+                const int s = s0 + i;
+                g[i] = 0.0f;
+                v[i] = make_uint4(0, 0, 0, 0);
+                if (s < k) {
+                    int64_t j = __ldg(inv_perm + t * k + s);
+                    if (j < 0 || j >= R) {
+                        bad = true;
+                        j = 0;
+                    }
+                    g[i] = gates ? __ldg(gates + t * k + s) : 1.0f;
+                    if (active) v[i] = ld_nc_v4(src + j * C + c0);
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < kCombineSlotBatch; ++i) {
+                if (s0 + i < k) {
+                    const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+#pragma unroll
+                    for (int h = 0; h < 4; ++h) {
+                        acc[2 * h] = fmaf(g[i], __uint_as_float(w[h] << 16), acc[2 * h]);
+                        acc[2 * h + 1] = fmaf(g[i], __uint_as_float(w[h] & 0xffff0000u),
+                                              acc[2 * h + 1]);
+                    }
+                }
+            }
+        }
+        if (active) {
+            uint4 o;
+            uint32_t* ow = reinterpret_cast<uint32_t*>(&o);
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+                __nv_bfloat162 b2 = __floats2bfloat162_rn(acc[2 * h], acc[2 * h + 1]);
+                ow[h] = *reinterpret_cast<uint32_t*>(&b2);
+            }
+            *reinterpret_cast<uint4*>(y + t * C + c0) = o;
+        }
+    }
+    if (bad) report(status, PK_ERR_BAD_INDEX);
+}
+
+namespace {
+int g_sms_cr[64] = {0};
+
+int sm_count() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    if (!g_sms_cr[dev]) cudaDeviceGetAttribute(&g_sms_cr[dev], cudaDevAttrMultiProcessorCount, dev);
+    return g_sms_cr[dev];
+}
+}  // namespace
+
+cudaError_t launch_router_topk(const float* logits, int32_t T, int32_t E, int32_t k,
+                               int32_t* topk, float* gates, cudaStream_t stream) {
+    if (T == 0) return cudaSuccess;
+    const int sms = sm_count();
+    if (!sms) return cudaErrorInvalidDevice;
+    const int64_t blocks = (static_cast<int64_t>(T) + 7) / 8;
+    const int grid = static_cast<int>(blocks < sms * 16 ? blocks : sms * 16);
+    k_router_topk<<<grid, 256, 0, stream>>>(logits, T, E, k, topk, gates);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_combine(const uint16_t* src, const int32_t* inv_perm, const float* gates,
+                           int32_t T, int32_t k, int32_t C, uint16_t* y, int32_t* status,
+                           cudaStream_t stream) {
+    if (T == 0) return cudaSuccess;
+    const int sms = sm_count();
+    if (!sms) return cudaErrorInvalidDevice;
+    const int64_t items = static_cast<int64_t>(T) * ((C + 255) / 256);
+    const int64_t blocks = (items + 7) / 8;
+    const int grid = static_cast<int>(blocks < sms * 8 ? blocks : sms * 8);
+    k_combine<<<grid, 256, 0, stream>>>(src, inv_perm, gates, T, k, C, y, status);
+    return cudaGetLastError();
+}
+
+}  // namespace pk

@@ -30,4 +30,10 @@ int launch_dispatch_gemm(const uint16_t* x, const int32_t* perm, const int32_t* 
 
 cudaError_t launch_bounded_wait_probe(int32_t* status, uint64_t limit_ns, cudaStream_t stream);
 
+cudaError_t launch_router_topk(const float* logits, int32_t T, int32_t E, int32_t k,
+                               int32_t* topk, float* gates, cudaStream_t stream);
+cudaError_t launch_combine(const uint16_t* src, const int32_t* inv_perm, const float* gates,
+                           int32_t T, int32_t k, int32_t C, uint16_t* y, int32_t* status,
+                           cudaStream_t stream);
+
 }  // namespace pk

@@ -16,7 +16,10 @@ claims", Fig. 17) restated for one device:
   increasing ``t*k+s`` inside each expert; and its inverse;
 * ``gemm_rows``     -- for sorted row ``j`` of expert ``e``:
   ``out[j, n] = sum_d x[perm[j] // k, d] * W[e, d, n]`` in float64 from the
-  bf16 inputs.
+  bf16 inputs;
+* ``combine``       -- ``y[t] = sum_s gates[t, s] * src[inv_perm[t*k+s]]``;
+* ``router_topk``   -- the k largest logits per token (ties to the lower
+  expert) and their softmax.
 
 Parity status: the pages print no worked example, so no function here is
 pinned to a value printed on the pages. Each is pinned instead by closed
@@ -41,7 +44,7 @@ def build(force: bool = False) -> str:
     if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
         tmp = _LIB + f".tmp{os.getpid()}"
         subprocess.check_call(["gcc", "-O2", "-std=c11", "-shared", "-fPIC", "-pthread",
-                               "-o", tmp, _SRC])
+                               "-o", tmp, _SRC, "-lm"])
         os.replace(tmp, _LIB)
     return _LIB
 
@@ -64,6 +67,10 @@ def _L():
         lib.oracle_build_perm.argtypes = [_P, _I, _I, _I, _P, _P, _P]
         lib.oracle_expert_of_row.restype = ctypes.c_int64
         lib.oracle_expert_of_row.argtypes = [_P, _I, _I]
+        lib.oracle_combine.restype = ctypes.c_int
+        lib.oracle_combine.argtypes = [_P, _P, _P, _I, _I, _I, _P]
+        lib.oracle_router_topk.restype = ctypes.c_int
+        lib.oracle_router_topk.argtypes = [_P, _I, _I, _I, _P, _P]
         lib.oracle_gemm_rows.restype = ctypes.c_int
         lib.oracle_gemm_rows.argtypes = [_P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _I, _P,
                                          ctypes.c_int]
@@ -136,6 +143,36 @@ def gemm_rows(x: np.ndarray, perm: np.ndarray, offsets: np.ndarray, W: np.ndarra
 
 def gemm_all(x, perm, offsets, W, k, threads=None) -> np.ndarray:
     return gemm_rows(x, perm, offsets, W, k, np.arange(perm.size), threads)
+
+
+def combine(src: np.ndarray, inv_perm: np.ndarray, gates: np.ndarray, T: int, k: int):
+    """float64 [T, C]: y[t] = sum_s gates[t, s] * src[inv_perm[t*k+s]] (s ascending)."""
+    src = _c(src, np.uint16)
+    R, C = src.shape
+    assert R == T * k
+    inv = _c(inv_perm, np.int64).reshape(-1)
+    g = _c(gates, np.float64).reshape(-1)
+    y = np.zeros((T, C), dtype=np.float64)
+    if T:
+        rc = _L().oracle_combine(src.ctypes.data, inv.ctypes.data, g.ctypes.data, T, k, C,
+                                 y.ctypes.data)
+        if rc:
+            raise OracleError("inv_perm entry outside [0, T*k)")
+    return y
+
+
+def router_topk(logits: np.ndarray, k: int):
+    """(topk int64 [T, k], gates float64 [T, k]) from float32 logits [T, E]."""
+    logits = _c(logits, np.float32)
+    T, E = logits.shape
+    topk = np.zeros((T, k), dtype=np.int64)
+    gates = np.zeros((T, k), dtype=np.float64)
+    if T:
+        rc = _L().oracle_router_topk(logits.ctypes.data, T, E, k, topk.ctypes.data,
+                                     gates.ctypes.data)
+        if rc:
+            raise OracleError("k outside [1, E]")
+    return topk, gates
 
 
 def bf16_to_f64(h: int) -> float:

@@ -22,6 +22,7 @@
  * All integer outputs are int64 so that nothing about their width is shared
  * with the device path (which uses int32).
  */
+#include <math.h>
 #include <pthread.h>
 #include <stdint.h>
 #include <stdlib.h>
@@ -142,4 +143,58 @@ int oracle_gemm_rows(const uint16_t* x, const int64_t* perm, const int64_t* offs
         status |= jobs[i].status;
     }
     return status;
+}
+
+/* ---------------------------------------------------------------------- */
+/* Combine (un-permute and weight) -- the step after the expert MLP in the
+ * expert-parallel token-dispatch + GEMM of "Loads and Loads of Fluffy
+ * Kittens" ("Key claims", Fig. 17), whose gating the pages leave open:
+ *   y[t][c] = sum over s = 0..k-1 of gates[t][s] * src[inv_perm[t*k + s]][c]
+ * with src in bf16 and the products and sum in float64, s ascending.
+ * Returns 0, or 1 if an inv_perm entry is outside [0, T*k). */
+int oracle_combine(const uint16_t* src, const int64_t* inv_perm, const double* gates, int64_t T,
+                   int64_t k, int64_t C, double* y) {
+    const int64_t R = T * k;
+    for (int64_t t = 0; t < T; ++t) {
+        for (int64_t c = 0; c < C; ++c) y[t * C + c] = 0.0;
+        for (int64_t s = 0; s < k; ++s) {
+            const int64_t j = inv_perm[t * k + s];
+            if (j < 0 || j >= R) return 1;
+            const double g = gates[t * k + s];
+            for (int64_t c = 0; c < C; ++c)
+                y[t * C + c] += g * oracle_bf16_to_f64(src[j * C + c]);
+        }
+    }
+    return 0;
+}
+
+/* Router top-k: for every token t, the k experts with the largest logits,
+ * largest first, equal logits going to the lower expert index; and gates =
+ * softmax over the k selected logits (float64, shifted by the largest).
+ * The pages fix top_k and num_experts ("Key claims", Fig. 17) but not the
+ * router; this is the plainest reading. */
+int oracle_router_topk(const float* logits, int64_t T, int64_t E, int64_t k, int64_t* topk,
+                       double* gates) {
+    if (k < 1 || k > E) return 1;
+    unsigned char* taken = (unsigned char*)malloc((size_t)E);
+    if (!taken) return 2;
+    for (int64_t t = 0; t < T; ++t) {
+        const float* l = logits + t * E;
+        for (int64_t e = 0; e < E; ++e) taken[e] = 0;
+        for (int64_t s = 0; s < k; ++s) {
+            int64_t best = -1;
+            for (int64_t e = 0; e < E; ++e) {
+                if (taken[e]) continue;
+                if (best < 0 || l[e] > l[best]) best = e;
+            }
+            taken[best] = 1;
+            topk[t * k + s] = best;
+        }
+        const double m = (double)l[topk[t * k]];
+        double z = 0.0;
+        for (int64_t s = 0; s < k; ++s) z += exp((double)l[topk[t * k + s]] - m);
+        for (int64_t s = 0; s < k; ++s) gates[t * k + s] = exp((double)l[topk[t * k + s]] - m) / z;
+    }
+    free(taken);
+    return 0;
 }

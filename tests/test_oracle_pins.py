@@ -275,3 +275,89 @@ def test_planted_gemm_mistakes_are_caught(bug):
         except AssertionError:
             caught += 1
     assert caught >= 1
+
+
+# ------------------------------------------------ combine and router pins
+def check_combine(comb, rng):
+    """Pins on comb(src_bits, inv_perm, gates, T, k) -> float64 [T, C]."""
+    T, k, E, C = 13, 3, 5, 24
+    topk = np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int32)
+    _, offsets = oracle.route_counts(topk, E)
+    perm, inv = oracle.build_perm(topk, E, offsets)
+    src = bf16(rng.standard_normal((T * k, C)).astype(np.float32))
+    sf = ig.bf16_bits_to_f64(src)
+    # one-hot gates pick a single expert output, exactly
+    for s in range(k):
+        g = np.zeros((T, k))
+        g[:, s] = 1.0
+        y = comb(src, inv, g, T, k)
+        assert np.array_equal(y, sf[inv.reshape(T, k)[:, s]])
+    # library reference: gather + einsum in float64
+    g = rng.random((T, k))
+    y = comb(src, inv, g, T, k)
+    ref = np.einsum("ts,tsc->tc", g, sf[inv.reshape(T, k)])
+    assert np.all(np.abs(y - ref) <= 1e-12 * (np.abs(g)[:, :, None] * np.abs(sf[inv.reshape(T, k)])).sum(1))
+    # dispatch followed by combine with unit gates and k = 1 restores the rows
+    tk1 = rng.integers(0, E, size=(T, 1)).astype(np.int32)
+    _, off1 = oracle.route_counts(tk1, E)
+    p1, i1 = oracle.build_perm(tk1, E, off1)
+    x = bf16(rng.standard_normal((T, C)).astype(np.float32))
+    dispatched = x[p1]                       # rows in sorted order
+    y = comb(dispatched, i1, np.ones((T, 1)), T, 1)
+    assert np.array_equal(y, ig.bf16_bits_to_f64(x))
+
+
+def check_router(router, rng):
+    """Pins on router(logits f32 [T,E], k) -> (topk, gates)."""
+    from scipy.special import softmax
+    T, E, k = 40, 37, 6
+    l = rng.standard_normal((T, E)).astype(np.float32)
+    idx, g = router(l, k)
+    assert np.array_equal(idx, np.argsort(-l, axis=1, kind="stable")[:, :k])
+    sel = np.take_along_axis(l.astype(np.float64), idx, axis=1)
+    assert np.allclose(g, softmax(sel, axis=1), rtol=1e-14, atol=0)
+    # ties go to the lower expert; equal logits give equal gates
+    l = np.zeros((3, 9), dtype=np.float32)
+    l[1, 4] = 1.0
+    idx, g = router(l, 4)
+    assert idx.tolist() == [[0, 1, 2, 3], [4, 0, 1, 2], [0, 1, 2, 3]]
+    assert np.all(g[0] == 0.25)
+    # k = E selects every expert once
+    idx, _ = router(rng.standard_normal((5, 7)).astype(np.float32), 7)
+    assert all(sorted(r) == list(range(7)) for r in idx.tolist())
+
+
+def test_combine_pins():
+    check_combine(lambda s, i, g, T, k: oracle.combine(s, i, g, T, k), np.random.default_rng(21))
+
+
+def test_router_pins():
+    check_router(oracle.router_topk, np.random.default_rng(22))
+
+
+def test_planted_combine_and_router_mistakes_are_caught():
+    def comb_perm_not_inv(src, inv, g, T, k):     # gathers with perm instead of inv_perm
+        perm = np.empty_like(inv)
+        perm[inv] = np.arange(inv.size)
+        return oracle.combine(src, perm, g, T, k)
+
+    def comb_gates_transposed(src, inv, g, T, k):
+        return oracle.combine(src, inv, np.ascontiguousarray(g[:, ::-1]), T, k)
+
+    def router_ties_high(l, k):                    # equal logits to the higher expert
+        idx = np.argsort(-l[:, ::-1], axis=1, kind="stable")[:, :k]
+        idx = l.shape[1] - 1 - idx
+        _, g = oracle.router_topk(l, k)
+        return idx, g
+
+    def router_no_shift(l, k):                     # gates of all experts, not the k selected
+        idx, _ = oracle.router_topk(l, k)
+        from scipy.special import softmax
+        return idx, softmax(l.astype(np.float64), axis=1)[np.arange(l.shape[0])[:, None], idx]
+
+    for bad in (comb_perm_not_inv, comb_gates_transposed):
+        with pytest.raises(AssertionError):
+            check_combine(bad, np.random.default_rng(21))
+    for bad in (router_ties_high, router_no_shift):
+        with pytest.raises(AssertionError):
+            check_router(bad, np.random.default_rng(22))
