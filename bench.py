@@ -407,6 +407,84 @@ def run_ours(args, wl):
     return line
 
 
+def run_op(args, wl):
+    """Timing of the kernels beside the dispatch + GEMM step (router top-k,
+    combine, down-projection grouped GEMM) on the workload's shapes."""
+    import torch
+    import inputgen as ig
+    import moe_token_dispatch_gb300 as pk
+
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream()
+    peaks, peak_kind = load_peaks()
+    R = wl.T * wl.k
+
+    def dev_bf16(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
+
+    # routing of the workload (GPU) for inv_perm / offsets
+    md = pk.MoeDispatch(wl.T, wl.k, wl.E, 8, 8, device=dev)
+    md.route(torch.from_numpy(ig.make_topk(wl)).to(dev))
+    torch.cuda.synchronize()
+    counts = md.counts.cpu().numpy()
+    if args.op == "router":
+        logits = torch.from_numpy(ig.make_logits(wl)).to(dev)
+        idx = torch.empty((wl.T, wl.k), dtype=torch.int32, device=dev)
+        g = torch.empty((wl.T, wl.k), dtype=torch.float32, device=dev)
+        fn = lambda: pk.pk_moe_router_topk(logits, wl.k, idx, g, stream)
+        alg_bytes, flops = wl.T * wl.E * 4 + wl.T * wl.k * 8, 0
+        metric = f"router top-k (fp32 logits -> top-{wl.k} of {wl.E} + softmax gates) at T={wl.T}"
+    elif args.op == "combine":
+        C = wl.D   # combine follows the down-projection: rows of the model width
+        src = dev_bf16(ig.make_src(wl, C))
+        gates = torch.from_numpy(ig.make_gates(wl)).to(dev)
+        y = torch.empty((wl.T, C), dtype=torch.bfloat16, device=dev)
+        fn = lambda: pk.pk_moe_combine(src, md.inv_perm, gates, wl.T, wl.k, y, md.status, stream)
+        alg_bytes, flops = R * C * 2 + wl.T * C * 2 + R * 4 + R * 4, 0
+        metric = f"combine y[t] = sum_s g[t,s] src[inv_perm[t*k+s]] at T={wl.T} k={wl.k} C={C}"
+    elif args.op == "grouped_gemm":
+        K, N = wl.De, wl.D   # down-projection: [R, D_expert] x W2[e] [D_expert, D]
+        A = dev_bf16(ig.normal_bf16(wl.seed, 7, 0, R * K).reshape(R, K))
+        W2 = dev_bf16(ig.make_W(ig.custom(T=wl.T, D=K, E=wl.E, k=wl.k, De=N, seed=wl.seed)))
+        out = torch.empty((R, N), dtype=torch.bfloat16, device=dev)
+        fn = lambda: pk.pk_moe_grouped_gemm(A, md.offsets, W2, out, md.status, stream)
+        touched = int((counts > 0).sum())
+        alg_bytes = R * K * 2 + touched * K * N * 2 + R * N * 2 + (wl.E + 1) * 4
+        flops = 2.0 * R * K * N
+        metric = (f"down-projection grouped GEMM TFLOP/s at R={R} K={K} N={N} E={wl.E}")
+    else:
+        raise SystemExit(f"unknown --op {args.op}")
+    for _ in range(max(3, args.warmup)):
+        fn()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    for a, b in ev:
+        a.record(stream)
+        fn()
+        b.record(stream)
+    torch.cuda.synchronize()
+    if md.status_code() != 0:
+        raise RuntimeError(f"device status {pk.pk_status_str(md.status_code())}")
+    ms = sorted(a.elapsed_time(b) for a, b in ev)
+    med = ms[len(ms) // 2]
+    gbs = alg_bytes / (med * 1e-3) / 1e9
+    line = {"op": args.op, "metric": metric, "workload": wl.name, "ms_median": med,
+            "ms_p10": ms[len(ms) // 10], "ms_p90": ms[(9 * len(ms)) // 10], "steps": args.steps,
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": gbs / peaks["hbm_gbs"], "algorithmic_bytes": alg_bytes,
+                         "peak_kind": peak_kind}}
+    if flops:
+        tf = flops / (med * 1e-3) / 1e12
+        line["value"], line["unit"] = tf, "TFLOP/s"
+        line["roofline"]["tensor"] = {"achieved": tf, "peak": peaks["bf16_tflops"],
+                                      "unit": "TFLOP/s", "frac": tf / peaks["bf16_tflops"]}
+    else:
+        line["value"], line["unit"] = gbs, "GB/s"
+    return line
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -415,6 +493,9 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="ep")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--op", default="dispatch_gemm",
+                    choices=["dispatch_gemm", "router", "combine", "grouped_gemm"],
+                    help="dispatch_gemm: the benchmark step; the others time one kernel")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)
 
@@ -430,7 +511,9 @@ def main(argv=None):
         else:
             if rank != 0:
                 return 0
-    if args.impl == "reference":
+    if args.op != "dispatch_gemm":
+        line = run_op(args, wl) if rank == 0 else None
+    elif args.impl == "reference":
         line = run_reference(args, wl)
     else:
         line = run_ours(args, wl)

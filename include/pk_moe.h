@@ -131,6 +131,22 @@ int pk_moe_dispatch_gemm(const uint16_t* x, const int32_t* perm, const int32_t* 
                          int32_t D_expert, uint16_t* out, int32_t* status_word, void* stream);
 
 /*
+ * Grouped GEMM of rows already in expert order -- the expert MLP's
+ * down-projection that follows the up-projection above (same expert
+ * segments; "Key claims", Fig. 17 gives D=7168, D_expert=2048): for every
+ * expert e and row j in [expert_offsets[e], expert_offsets[e+1]),
+ *   out[j, n] = bf16_rne( sum_c A[j, c] * W[e, c, n] )
+ * with fp32 accumulation on the tensor cores.
+ *   A        device bf16 [R, K] (row j of expert segment e), 16-byte aligned
+ *   W        device bf16 [E, K, N], 16-byte aligned
+ *   out      device bf16 [R, N], 16-byte aligned; rows of each segment written
+ * Requires K and N multiples of 8. Offsets are clamped into [0, R].
+ */
+int pk_moe_grouped_gemm(const uint16_t* A, const int32_t* expert_offsets, const uint16_t* W,
+                        int32_t R, int32_t K, int32_t N, int32_t E, uint16_t* out,
+                        int32_t* status_word, void* stream);
+
+/*
  * Router top-k (the selection the expert-parallel workload of "Key claims",
  * Fig. 17 describes with top_k=8 of num_experts=256; the pages leave the
  * router itself open): for every token t,

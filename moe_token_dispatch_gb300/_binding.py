@@ -51,6 +51,8 @@ def _load():
     lib.pk_moe_dispatch_gemm.argtypes = [P, P, P, P, I32, I32, I32, I32, I32, P, P, P]
     lib.pk_moe_route_noalloc.restype = ctypes.c_int
     lib.pk_moe_route_noalloc.argtypes = [P, I32, I32, I32, P, P, P, P, P, P]
+    lib.pk_moe_grouped_gemm.restype = ctypes.c_int
+    lib.pk_moe_grouped_gemm.argtypes = [P, P, P, I32, I32, I32, I32, P, P, P]
     lib.pk_moe_router_topk.restype = ctypes.c_int
     lib.pk_moe_router_topk.argtypes = [P, I32, I32, I32, P, P, P]
     lib.pk_moe_combine.restype = ctypes.c_int
@@ -156,6 +158,21 @@ def pk_moe_dispatch_gemm(x: torch.Tensor, perm: torch.Tensor, expert_offsets: to
         _ptr(out, torch.bfloat16, "out", T * k * De),
         _ptr(status_word, torch.int32, "status_word", 1), _stream(stream))
     _check(rc, "pk_moe_dispatch_gemm")
+
+
+def pk_moe_grouped_gemm(A: torch.Tensor, expert_offsets: torch.Tensor, W: torch.Tensor,
+                        out: torch.Tensor, status_word: torch.Tensor | None = None,
+                        stream=None) -> None:
+    R, K = A.shape
+    E, K2, N = W.shape
+    if K2 != K:
+        raise ValueError(f"W is [E, {K2}, N] but A has K={K}")
+    rc = lib.pk_moe_grouped_gemm(_ptr(A, torch.bfloat16, "A"),
+                                 _ptr(expert_offsets, torch.int32, "expert_offsets", E + 1),
+                                 _ptr(W, torch.bfloat16, "W"), R, K, N, E,
+                                 _ptr(out, torch.bfloat16, "out", R * N),
+                                 _ptr(status_word, torch.int32, "status_word", 1), _stream(stream))
+    _check(rc, "pk_moe_grouped_gemm")
 
 
 def pk_moe_router_topk(logits: torch.Tensor, k: int, topk_idx: torch.Tensor,

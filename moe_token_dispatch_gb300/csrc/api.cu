@@ -89,6 +89,19 @@ int pk_moe_dispatch_gemm(const uint16_t* x, const int32_t* perm, const int32_t* 
                                     g_wait_limit_ns.load(std::memory_order_relaxed));
 }
 
+int pk_moe_grouped_gemm(const uint16_t* A, const int32_t* expert_offsets, const uint16_t* W,
+                        int32_t R, int32_t K, int32_t N, int32_t E, uint16_t* out,
+                        int32_t* status_word, void* stream) {
+    if (R < 0 || K < 1 || N < 1 || E < 1) return PK_ERR_INVALID_ARG;
+    if ((K % 8) != 0 || (N % 8) != 0) return PK_ERR_INVALID_ARG;
+    if (R == 0) return PK_OK;
+    if (!A || !expert_offsets || !W || !out) return PK_ERR_INVALID_ARG;
+    if (!aligned16(A) || !aligned16(W) || !aligned16(out)) return PK_ERR_INVALID_ARG;
+    return pk::launch_grouped_gemm(A, expert_offsets, W, R, K, N, E, out, status_word,
+                                   static_cast<cudaStream_t>(stream),
+                                   g_wait_limit_ns.load(std::memory_order_relaxed));
+}
+
 int pk_moe_router_topk(const float* logits, int32_t T, int32_t E, int32_t k, int32_t* topk_idx,
                        float* gates, void* stream) {
     if (T < 0 || E < 1 || k < 1 || k > E || k > 32) return PK_ERR_INVALID_ARG;

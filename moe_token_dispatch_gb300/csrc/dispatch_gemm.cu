@@ -29,6 +29,11 @@
 // warps off the MMA issuer's sub-partition.
 // Three 64 KiB stages (full/empty mbarriers) connect producers and MMA.
 //
+// The same kernel, instantiated with kGather = false, is the grouped GEMM of
+// rows that are already in expert order (the down-projection that follows the
+// expert MLP: out2[j, :] = h[j, :] @ W2[e(j)]): the W producer then also
+// TMA-loads each m-tile of A as one 128-row box, and the gather warps idle.
+//
 // Work unit = (expert e, group of m-tiles, n-tile), with a shape chosen per
 // expert so that TMEM (512 fp32 columns x 128 lanes) holds every accumulator
 // of the unit and each W tile is loaded once per unit:
@@ -193,8 +198,10 @@ __device__ __forceinline__ void store_row_chunk(uint16_t* dst, const uint32_t (&
     }
 }
 
+template <bool kGather>
 __global__ void __launch_bounds__(THREADS, 1)
-    k_dispatch_gemm(const __grid_constant__ CUtensorMap wmap, const uint16_t* __restrict__ x,
+    k_dispatch_gemm(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap amap,
+                    const uint16_t* __restrict__ x,
                     const int32_t* __restrict__ perm, const int32_t* __restrict__ offsets,
                     uint16_t* __restrict__ out, int32_t T, int32_t k, int32_t D, int32_t E,
                     int32_t De, int32_t* status, uint64_t limit) {
@@ -217,7 +224,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
-            mbar_init(full0 + 8 * s, 1 + GATHER_THREADS);
+            mbar_init(full0 + 8 * s, kGather ? 1 + GATHER_THREADS : 1);
             mbar_init(empty0 + 8 * s, 1);
         }
         mbar_init(acc_full, 1);
@@ -226,7 +233,10 @@ __global__ void __launch_bounds__(THREADS, 1)
         ctl->abort = 0;
         fence_barrier_init();
     }
-    if (warp == W_WARP && lane == 0) prefetch_tensormap(&wmap);
+    if (warp == W_WARP && lane == 0) {
+        prefetch_tensormap(&wmap);
+        if (!kGather) prefetch_tensormap(&amap);
+    }
     if (warp == MMA_WARP) {
         tmem_alloc(smem_addr(&ctl->tmem_base), TMEM_COLS);
         tmem_relinquish();
@@ -236,8 +246,10 @@ __global__ void __launch_bounds__(THREADS, 1)
     tc_fence_after_sync();
     const uint32_t tmem = ctl->tmem_base;
 
+    // Without kGather the rows arrive by TMA (W producer) and warps 6, 7, 9,
+    // 10 fall through to the final barrier.
     const int gt = gather_index(warp, lane);
-    if (gt >= 0) {
+    if (kGather && gt >= 0) {
         // ------------------------------------------------------ dispatch
         const int c = gt & 7;          // 16-byte chunk of the 128-byte row segment
         const int rb = gt >> 3;        // first row of this thread (0..15)
@@ -300,7 +312,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         // ----------------------------------------------------- W producer
         if (lane == 0) {
             const uint64_t pol_once = policy_evict_first();
-            const uint64_t pol_reuse = policy_evict_last();
+            const uint64_t pol_reuse = policy_evict_last();  // also A: re-read by every n-tile
             Walker wk, pf;
             wk.init(offsets, E, R, De);
             pf.init(offsets, E, R, De);
@@ -328,6 +340,9 @@ __global__ void __launch_bounds__(THREADS, 1)
                 if (!wk.find(u, U)) break;
                 const int nbox = U.bn / B_BOX;
                 const uint64_t pol = U.shared_w ? pol_reuse : pol_once;
+                const uint32_t a_off = static_cast<uint32_t>(U.bn_max) * (BK * 2);
+                const uint32_t tx = static_cast<uint32_t>(nbox * B_BOX_BYTES) +
+                                    (kGather ? 0u : static_cast<uint32_t>(U.mpu * A_BYTES));
                 for (int ks = 0; ks < nk; ++ks) {
                     prefetch_one();
                     if (!mbar_wait(empty0 + 8 * stage, phase ^ 1u, abort, limit)) {
@@ -336,11 +351,15 @@ __global__ void __launch_bounds__(THREADS, 1)
                         break;
                     }
                     const uint32_t full = full0 + 8 * stage;
-                    mbar_arrive_expect_tx(full, static_cast<uint32_t>(nbox) * B_BOX_BYTES);
+                    mbar_arrive_expect_tx(full, tx);
                     const uint32_t sb = sbase + stage * STAGE_BYTES;
                     for (int b = 0; b < nbox; ++b)
                         tma_load_3d(sb + b * B_BOX_BYTES, &wmap, U.n0 + b * B_BOX, ks * BK, U.e,
                                     full, pol);
+                    if (!kGather)  // rows past the expert's end are loaded but never stored
+                        for (int mt = 0; mt < U.mpu; ++mt)
+                            tma_load_2d(sb + a_off + mt * A_BYTES, &amap, ks * BK, U.row0 + mt * BM,
+                                        full, pol_reuse);
                     issued |= 1u << stage;
                     issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
                     if (++stage == STAGES) {
@@ -511,10 +530,13 @@ PFN_cuTensorMapEncodeTiled_v12000 encoder() {
 
 }  // namespace
 
-int launch_dispatch_gemm(const uint16_t* x, const int32_t* perm, const int32_t* offsets,
-                         const uint16_t* W, int32_t T, int32_t k, int32_t D, int32_t E,
-                         int32_t De, uint16_t* out, int32_t* status, cudaStream_t stream,
-                         uint64_t wait_limit_ns) {
+namespace {
+
+// Builds the tensor maps and launches one instantiation. A is x (gathered
+// through perm) or, without gather, the [T, D] matrix of expert-sorted rows.
+int launch_common(bool gather, const uint16_t* A, const int32_t* perm, const int32_t* offsets,
+                  const uint16_t* W, int32_t T, int32_t k, int32_t D, int32_t E, int32_t De,
+                  uint16_t* out, int32_t* status, cudaStream_t stream, uint64_t wait_limit_ns) {
     using namespace dg;
     auto enc = encoder();
     if (!enc) return PK_ERR_CUDA;
@@ -527,7 +549,11 @@ int launch_dispatch_gemm(const uint16_t* x, const int32_t* perm, const int32_t* 
         if (!di.attr_set) {
             if (cudaDeviceGetAttribute(&di.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
                 return PK_ERR_CUDA;
-            if (cudaFuncSetAttribute(k_dispatch_gemm, cudaFuncAttributeMaxDynamicSharedMemorySize,
+            if (cudaFuncSetAttribute(k_dispatch_gemm<true>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     SMEM_BYTES) != cudaSuccess ||
+                cudaFuncSetAttribute(k_dispatch_gemm<false>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      SMEM_BYTES) != cudaSuccess)
                 return PK_ERR_CUDA;
             di.attr_set = true;
@@ -535,7 +561,7 @@ int launch_dispatch_gemm(const uint16_t* x, const int32_t* perm, const int32_t* 
         sms = di.sms;
     }
 
-    CUtensorMap wmap;
+    CUtensorMap wmap, amap;
     {
         cuuint64_t dims[3] = {static_cast<cuuint64_t>(De), static_cast<cuuint64_t>(D),
                               static_cast<cuuint64_t>(E)};
@@ -548,9 +574,43 @@ int launch_dispatch_gemm(const uint16_t* x, const int32_t* perm, const int32_t* 
                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return PK_ERR_UNSUPPORTED;
     }
-    k_dispatch_gemm<<<sms, THREADS, SMEM_BYTES, stream>>>(wmap, x, perm, offsets, out, T, k, D, E,
-                                                         De, status, wait_limit_ns);
+    if (gather) {
+        amap = wmap;  // unused
+    } else {
+        // A [T, D] row-major, boxes of 64 columns x 128 rows, 128-byte swizzle
+        cuuint64_t dims[2] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(T)};
+        cuuint64_t strides[1] = {static_cast<cuuint64_t>(D) * 2};
+        cuuint32_t box[2] = {BK, BM};
+        cuuint32_t es[2] = {1, 1};
+        if (enc(&amap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(A), dims, strides,
+                box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return PK_ERR_UNSUPPORTED;
+    }
+    if (gather)
+        k_dispatch_gemm<true><<<sms, THREADS, SMEM_BYTES, stream>>>(
+            wmap, amap, A, perm, offsets, out, T, k, D, E, De, status, wait_limit_ns);
+    else
+        k_dispatch_gemm<false><<<sms, THREADS, SMEM_BYTES, stream>>>(
+            wmap, amap, A, perm, offsets, out, T, k, D, E, De, status, wait_limit_ns);
     return cudaGetLastError() == cudaSuccess ? PK_OK : PK_ERR_CUDA;
+}
+
+}  // namespace
+
+int launch_dispatch_gemm(const uint16_t* x, const int32_t* perm, const int32_t* offsets,
+                         const uint16_t* W, int32_t T, int32_t k, int32_t D, int32_t E,
+                         int32_t De, uint16_t* out, int32_t* status, cudaStream_t stream,
+                         uint64_t wait_limit_ns) {
+    return launch_common(true, x, perm, offsets, W, T, k, D, E, De, out, status, stream,
+                         wait_limit_ns);
+}
+
+int launch_grouped_gemm(const uint16_t* A, const int32_t* offsets, const uint16_t* W, int32_t R,
+                        int32_t K, int32_t N, int32_t E, uint16_t* out, int32_t* status,
+                        cudaStream_t stream, uint64_t wait_limit_ns) {
+    return launch_common(false, A, nullptr, offsets, W, R, 1, K, E, N, out, status, stream,
+                         wait_limit_ns);
 }
 
 // ------------------------------------------------- bounded-wait check kernel

@@ -28,6 +28,11 @@ int launch_dispatch_gemm(const uint16_t* x, const int32_t* perm, const int32_t* 
                          int32_t De, uint16_t* out, int32_t* status, cudaStream_t stream,
                          uint64_t wait_limit_ns);
 
+// Grouped GEMM of expert-sorted rows (no gather).
+int launch_grouped_gemm(const uint16_t* A, const int32_t* offsets, const uint16_t* W, int32_t R,
+                        int32_t K, int32_t N, int32_t E, uint16_t* out, int32_t* status,
+                        cudaStream_t stream, uint64_t wait_limit_ns);
+
 cudaError_t launch_bounded_wait_probe(int32_t* status, uint64_t limit_ns, cudaStream_t stream);
 
 cudaError_t launch_router_topk(const float* logits, int32_t T, int32_t E, int32_t k,

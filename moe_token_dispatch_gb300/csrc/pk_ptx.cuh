@@ -292,3 +292,15 @@ __device__ __forceinline__ void mma_commit_multicast(uint32_t bar, uint16_t cta_
 }
 
 }  // namespace pk
+
+namespace pk {
+// Tiled 2-D load of one box into shared memory; completion counted on `bar`.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int c0, int c1,
+                                            uint32_t bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cta.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+        "l"(map), "r"(c0), "r"(c1), "r"(bar), "l"(policy)
+        : "memory");
+}
+}  // namespace pk

@@ -109,3 +109,55 @@ def test_combine_bad_index_sets_status(gpu_lib):
     inv[5] = T * k + 3
     _, st = _combine_gpu(gpu_lib, src, inv, np.ones((T, k), np.float32), T, k)
     assert st == gpu_lib.PK_ERR_BAD_INDEX
+
+
+# ------------------------------------------------ grouped (down-projection) GEMM
+def _grouped_case(R_T, K, E, k, N, seed=0, zipf=0.0):
+    """Rows of A in expert order from a routing, and W2 [E, K, N]."""
+    wl = ig.custom(T=R_T, D=K, E=E, k=k, De=N, zipf_s=zipf, seed=seed)
+    topk = ig.make_topk(wl)
+    counts, offsets = oracle.route_counts(topk, E)
+    R = R_T * k
+    A = ig.normal_bf16(seed, 7, 0, R * K).reshape(R, K)
+    W = ig.make_W(wl)
+    return A, offsets, W
+
+
+def _check_grouped(pk, A, offsets, W, rows=None):
+    from _gpu_util import assert_gemm_close
+    R, K = A.shape
+    E, _, N = W.shape
+    Ad, Wd = u16_to_bf16_dev(A), u16_to_bf16_dev(W)
+    off = torch.from_numpy(offsets.astype(np.int32)).cuda()
+    out = torch.zeros((R, N), dtype=torch.bfloat16, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pk.pk_moe_grouped_gemm(Ad, off, Wd, out, st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    if rows is None:
+        rows = np.arange(R)
+    # rows already in expert order: the oracle's GEMM with the identity permutation, k = 1
+    ref = oracle.gemm_rows(A, np.arange(R), offsets, W, 1, rows)
+    got = bf16_dev_to_f64(out[torch.from_numpy(rows).cuda()])
+    assert_gemm_close(got, ref, rows)
+
+
+@pytest.mark.parametrize("T,K,E,k,N", [(512, 576, 4, 2, 640), (700, 200, 3, 1, 200),
+                                       (300, 2048, 8, 3, 1408), (96, 8, 5, 2, 8),
+                                       (1000, 64, 2, 2, 256)])
+def test_grouped_gemm_all_rows(gpu_lib, T, K, E, k, N):
+    A, offsets, W = _grouped_case(T, K, E, k, N)
+    _check_grouped(gpu_lib, A, offsets, W)
+
+
+def test_grouped_gemm_down_projection_shape(gpu_lib):
+    # the ep down-projection: K = D_expert = 2048, N = D = 7168, 256 experts
+    from _gpu_util import boundary_rows
+    A, offsets, W = _grouped_case(8192, 2048, 256, 8, 7168)
+    rows = boundary_rows(offsets, np.random.default_rng(3), 128)
+    _check_grouped(gpu_lib, A, offsets, W, rows)
+
+
+def test_grouped_gemm_skewed(gpu_lib):
+    A, offsets, W = _grouped_case(2048, 256, 32, 4, 384, zipf=1.2)
+    _check_grouped(gpu_lib, A, offsets, W)
