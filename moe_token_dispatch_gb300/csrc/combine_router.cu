@@ -21,40 +21,39 @@
 namespace pk {
 
 // ------------------------------------------------------------------ router
-constexpr int kRouterMaxPerLane = PK_ROUTER_MAX_EXPERTS / 32;
-
+// PER = logits held per lane (E <= 32 * PER), a power of two so that the
+// selection loops are fully unrolled for the common expert counts.
+template <int PER>
 __global__ void __launch_bounds__(256)
     k_router_topk(const float* __restrict__ logits, int32_t T, int32_t E, int32_t k,
                   int32_t* __restrict__ topk, float* __restrict__ gates) {
+    constexpr int kNone = 0x7fffffff;
     const int lane = threadIdx.x & 31;
     const int64_t warp0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
-    const int per = (E + 31) / 32;
     for (int64_t t = warp0; t < T; t += nwarps) {
         const float* row = logits + t * E;
-        float v[kRouterMaxPerLane];
+        float v[PER];
+        uint32_t avail = 0;  // bit i: entry i of this lane exists and is not taken
 #pragma unroll
-        for (int i = 0; i < kRouterMaxPerLane; ++i) {
+        for (int i = 0; i < PER; ++i) {
             const int e = i * 32 + lane;
-            v[i] = (i < per && e < E) ? __ldg(row + e) : -INFINITY;
+            v[i] = e < E ? __ldg(row + e) : -INFINITY;
+            if (e < E) avail |= 1u << i;
         }
-        uint32_t taken = 0;
         float my_val = -INFINITY;
         int my_idx = 0;
         for (int s = 0; s < k; ++s) {
-            // this lane's best untaken entry; e grows with i, so replacing only
-            // on a strictly larger value keeps the lowest index among equals
-            constexpr int kNone = 0x7fffffff;
+            // this lane's best available entry; e grows with i, so replacing
+            // only on a strictly larger value keeps the lowest index among equals
             float bv = -INFINITY;
             int bi = kNone;
 #pragma unroll
-            for (int i = 0; i < kRouterMaxPerLane; ++i) {
-                const int e = i * 32 + lane;
-                if (i < per && e < E && !((taken >> i) & 1u) && (bi == kNone || v[i] > bv)) {
+            for (int i = 0; i < PER; ++i)
+                if (((avail >> i) & 1u) && (bi == kNone || v[i] > bv)) {
                     bv = v[i];
-                    bi = e;
+                    bi = i * 32 + lane;
                 }
-            }
             for (int d = 16; d > 0; d >>= 1) {
                 const float ov = __shfl_xor_sync(0xffffffffu, bv, d);
                 const int oi = __shfl_xor_sync(0xffffffffu, bi, d);
@@ -63,7 +62,7 @@ __global__ void __launch_bounds__(256)
                     bi = oi;
                 }
             }
-            if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+            if ((bi & 31) == lane) avail &= ~(1u << (bi >> 5));
             if (lane == s) {
                 my_val = bv;
                 my_idx = bi;
@@ -173,7 +172,19 @@ cudaError_t launch_router_topk(const float* logits, int32_t T, int32_t E, int32_
     if (!sms) return cudaErrorInvalidDevice;
     const int64_t blocks = (static_cast<int64_t>(T) + 7) / 8;
     const int grid = static_cast<int>(blocks < sms * 16 ? blocks : sms * 16);
-    k_router_topk<<<grid, 256, 0, stream>>>(logits, T, E, k, topk, gates);
+    const int per = (E + 31) / 32;
+    if (per <= 1)
+        k_router_topk<1><<<grid, 256, 0, stream>>>(logits, T, E, k, topk, gates);
+    else if (per <= 2)
+        k_router_topk<2><<<grid, 256, 0, stream>>>(logits, T, E, k, topk, gates);
+    else if (per <= 4)
+        k_router_topk<4><<<grid, 256, 0, stream>>>(logits, T, E, k, topk, gates);
+    else if (per <= 8)
+        k_router_topk<8><<<grid, 256, 0, stream>>>(logits, T, E, k, topk, gates);
+    else if (per <= 16)
+        k_router_topk<16><<<grid, 256, 0, stream>>>(logits, T, E, k, topk, gates);
+    else
+        k_router_topk<32><<<grid, 256, 0, stream>>>(logits, T, E, k, topk, gates);
     return cudaGetLastError();
 }
 
