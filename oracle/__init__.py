@@ -19,7 +19,10 @@ claims", Fig. 17) restated for one device:
   bf16 inputs;
 * ``combine``       -- ``y[t] = sum_s gates[t, s] * src[inv_perm[t*k+s]]``;
 * ``router_topk``   -- the k largest logits per token (ties to the lower
-  expert) and their softmax.
+  expert) and their softmax;
+* ``quant_rows`` / ``quant_cols`` / ``gemm_fp8_rows`` -- E4M3 quantisation
+  with one float32 scale per row of x and per output column of W, and the
+  expert GEMM on the codes.
 
 Parity status: the pages print no worked example, so no function here is
 pinned to a value printed on the pages. Each is pinned instead by closed
@@ -71,6 +74,17 @@ def _L():
         lib.oracle_combine.argtypes = [_P, _P, _P, _I, _I, _I, _P]
         lib.oracle_router_topk.restype = ctypes.c_int
         lib.oracle_router_topk.argtypes = [_P, _I, _I, _I, _P, _P]
+        lib.oracle_f32_to_e4m3.restype = ctypes.c_uint8
+        lib.oracle_f32_to_e4m3.argtypes = [ctypes.c_float]
+        lib.oracle_e4m3_to_f64.restype = ctypes.c_double
+        lib.oracle_e4m3_to_f64.argtypes = [ctypes.c_uint8]
+        lib.oracle_quant_rows.restype = None
+        lib.oracle_quant_rows.argtypes = [_P, _I, _I, _P, _P]
+        lib.oracle_quant_cols.restype = None
+        lib.oracle_quant_cols.argtypes = [_P, _I, _I, _I, _P, _P]
+        lib.oracle_gemm_fp8_rows.restype = ctypes.c_int
+        lib.oracle_gemm_fp8_rows.argtypes = [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _I,
+                                             _P]
         lib.oracle_gemm_rows.restype = ctypes.c_int
         lib.oracle_gemm_rows.argtypes = [_P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _I, _P,
                                          ctypes.c_int]
@@ -173,6 +187,59 @@ def router_topk(logits: np.ndarray, k: int):
         if rc:
             raise OracleError("k outside [1, E]")
     return topk, gates
+
+
+def f32_to_e4m3(v: float) -> int:
+    return int(_L().oracle_f32_to_e4m3(v))
+
+
+def e4m3_to_f64(c: int) -> float:
+    return float(_L().oracle_e4m3_to_f64(c))
+
+
+def quant_rows(x: np.ndarray):
+    """E4M3 codes [T, D] (uint8) and fp32 scales [T] of the rows of bf16 x."""
+    x = _c(x, np.uint16)
+    T, D = x.shape
+    q = np.zeros((T, D), dtype=np.uint8)
+    s = np.zeros(T, dtype=np.float32)
+    if T:
+        _L().oracle_quant_rows(x.ctypes.data, T, D, q.ctypes.data, s.ctypes.data)
+    return q, s
+
+
+def quant_cols(W: np.ndarray):
+    """E4M3 codes [E, N, D] (each output column contiguous) and fp32 scales
+    [E, N] of the columns of bf16 W [E, D, N]."""
+    W = np.asarray(W)
+    assert W.dtype == np.uint16 and W.flags.c_contiguous
+    E, D, N = W.shape
+    q = np.zeros((E, N, D), dtype=np.uint8)
+    s = np.zeros((E, N), dtype=np.float32)
+    _L().oracle_quant_cols(W.ctypes.data, E, D, N, q.ctypes.data, s.ctypes.data)
+    return q, s
+
+
+def gemm_fp8_rows(xq, sx, perm, offsets, wq, sw, k, rows) -> np.ndarray:
+    """float64 [len(rows), N] of the FP8 expert GEMM from codes and scales."""
+    xq = _c(xq, np.uint8)
+    sx = _c(sx, np.float32)
+    wq = np.asarray(wq)
+    assert wq.dtype == np.uint8 and wq.flags.c_contiguous
+    sw = _c(sw, np.float32)
+    T, D = xq.shape
+    E, N, D2 = wq.shape
+    assert D2 == D
+    perm = _c(perm, np.int64)
+    offsets = _c(offsets, np.int64)
+    rows = _c(np.asarray(rows).reshape(-1), np.int64)
+    out = np.zeros((rows.size, N), dtype=np.float64)
+    if rows.size and _L().oracle_gemm_fp8_rows(xq.ctypes.data, sx.ctypes.data, perm.ctypes.data,
+                                               offsets.ctypes.data, wq.ctypes.data, sw.ctypes.data,
+                                               T, k, D, E, N, rows.ctypes.data, rows.size,
+                                               out.ctypes.data):
+        raise OracleError("row outside every expert segment, or token out of range")
+    return out
 
 
 def bf16_to_f64(h: int) -> float:

@@ -198,3 +198,92 @@ int oracle_router_topk(const float* logits, int64_t T, int64_t E, int64_t k, int
     free(taken);
     return 0;
 }
+
+/* ---------------------------------------------------------------------- */
+/* FP8 (E4M3) weights and activations: the "FP8 weights" variant of the
+ * expert GEMM (the pages mention FP8 tensor-core support for Blackwell only
+ * in passing; the quantisation scheme here is a reading). Codes follow the
+ * OCP 8-bit floating point E4M3 format: 1 sign bit, 4 exponent bits (bias 7),
+ * 3 mantissa bits, largest finite 448, no infinities, NaN = S.1111.111.
+ * Conversion: round to nearest, ties to even; magnitudes above 448 saturate
+ * to 448 (as the hardware's satfinite conversion does). */
+uint8_t oracle_f32_to_e4m3(float f) {
+    const uint8_t sign = signbit(f) ? 0x80u : 0u;
+    if (isnan(f)) return (uint8_t)(sign | 0x7Fu);
+    const double a = fabs((double)f);
+    if (a >= 448.0) return (uint8_t)(sign | 0x7Eu);
+    if (a < 0.015625) { /* below the smallest normal 2^-6: steps of 2^-9 */
+        const double m = rint(a * 512.0); /* 0..8; 8 is the smallest normal */
+        return (uint8_t)(sign | (uint8_t)m);
+    }
+    int e = (int)floor(log2(a));
+    if (ldexp(1.0, e) > a) e -= 1;          /* guard log2 rounding */
+    if (ldexp(1.0, e + 1) <= a) e += 1;
+    double m = rint((a / ldexp(1.0, e) - 1.0) * 8.0); /* 0..8 */
+    if (m >= 8.0) { m = 0.0; e += 1; }
+    uint32_t code = (uint32_t)((e + 7) << 3) | (uint32_t)m;
+    if (code > 0x7Eu) code = 0x7Eu;
+    return (uint8_t)(sign | code);
+}
+
+double oracle_e4m3_to_f64(uint8_t c) {
+    const double s = (c & 0x80u) ? -1.0 : 1.0;
+    const int e = (c >> 3) & 0xF, m = c & 7;
+    if (e == 15 && m == 7) return NAN;
+    if (e == 0) return s * ldexp((double)m, -9);
+    return s * ldexp(1.0 + m / 8.0, e - 7);
+}
+
+/* One vector quantised with one scale, in float32 arithmetic:
+ *   amax = max |v|,  inv = 448 / amax,  code = E4M3(v * inv),
+ *   scale = amax / 448   (amax == 0: inv = scale = 1). */
+static void quant_vec(const uint16_t* v, int64_t n, int64_t stride, uint8_t* q, int64_t qstride,
+                      float* scale) {
+    float amax = 0.0f;
+    for (int64_t i = 0; i < n; ++i) {
+        const float a = fabsf((float)oracle_bf16_to_f64(v[i * stride]));
+        if (a > amax) amax = a;
+    }
+    const float inv = amax > 0.0f ? 448.0f / amax : 1.0f;
+    *scale = amax > 0.0f ? amax / 448.0f : 1.0f;
+    for (int64_t i = 0; i < n; ++i)
+        q[i * qstride] = oracle_f32_to_e4m3((float)oracle_bf16_to_f64(v[i * stride]) * inv);
+}
+
+/* Rows of x [T, D]: xq [T, D], sx [T]. */
+void oracle_quant_rows(const uint16_t* x, int64_t T, int64_t D, uint8_t* xq, float* sx) {
+    for (int64_t t = 0; t < T; ++t) quant_vec(x + t * D, D, 1, xq + t * D, 1, sx + t);
+}
+
+/* Columns of every W[e] [D, N]: codes stored transposed, wq [E, N, D] (each
+ * output column's D codes contiguous), sw [E, N]. */
+void oracle_quant_cols(const uint16_t* W, int64_t E, int64_t D, int64_t N, uint8_t* wq,
+                       float* sw) {
+    for (int64_t e = 0; e < E; ++e)
+        for (int64_t n = 0; n < N; ++n)
+            quant_vec(W + e * D * N + n, D, N, wq + (e * N + n) * D, 1, sw + e * N + n);
+}
+
+/* The FP8 expert GEMM for the listed sorted rows, float64 from the codes:
+ *   out[j][n] = (sum_d q(x)[t][d] * q(W)[e][n][d]) * sx[t] * sw[e][n],
+ * t = perm[j] / k, e = e(j). */
+int oracle_gemm_fp8_rows(const uint8_t* xq, const float* sx, const int64_t* perm,
+                         const int64_t* offsets, const uint8_t* wq, const float* sw, int64_t T,
+                         int64_t k, int64_t D, int64_t E, int64_t N, const int64_t* rows,
+                         int64_t nrows, double* out) {
+    for (int64_t r = 0; r < nrows; ++r) {
+        const int64_t j = rows[r];
+        const int64_t e = oracle_expert_of_row(offsets, E, j);
+        if (e < 0) return 1;
+        const int64_t t = perm[j] / k;
+        if (t < 0 || t >= T) return 1;
+        for (int64_t n = 0; n < N; ++n) {
+            const uint8_t* wcol = wq + (e * N + n) * D;
+            double acc = 0.0;
+            for (int64_t d = 0; d < D; ++d)
+                acc += oracle_e4m3_to_f64(xq[t * D + d]) * oracle_e4m3_to_f64(wcol[d]);
+            out[r * N + n] = acc * (double)sx[t] * (double)sw[e * N + n];
+        }
+    }
+    return 0;
+}

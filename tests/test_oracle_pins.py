@@ -361,3 +361,95 @@ def test_planted_combine_and_router_mistakes_are_caught():
     for bad in (router_ties_high, router_no_shift):
         with pytest.raises(AssertionError):
             check_router(bad, np.random.default_rng(22))
+
+
+# ------------------------------------------------------------- FP8 pins
+def test_e4m3_conversion_against_torch_and_format():
+    import torch
+    # every finite code round-trips, and the values follow the format
+    for c in range(256):
+        if (c & 0x7F) == 0x7F:
+            assert math.isnan(oracle.e4m3_to_f64(c))
+            continue
+        v = oracle.e4m3_to_f64(c)
+        assert oracle.f32_to_e4m3(v) == (c if v != 0 or c == 0 else c)
+    assert oracle.e4m3_to_f64(0x7E) == 448.0 and oracle.e4m3_to_f64(0x01) == 2.0 ** -9
+    # round to nearest even on random in-range floats: torch's cast (library)
+    rng = np.random.default_rng(31)
+    v = np.concatenate([rng.standard_normal(20000) * 30, rng.standard_normal(5000) * 1e-2,
+                        (rng.integers(-60, 60, 2000) + 0.5) / 8.0]).astype(np.float32)
+    v = v[np.abs(v) < 448]
+    ref = torch.from_numpy(v).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    ours = np.array([oracle.f32_to_e4m3(float(a)) for a in v], dtype=np.uint8)
+    assert np.array_equal(ours, ref)
+    # saturation above the largest finite value
+    assert oracle.f32_to_e4m3(1e6) == 0x7E and oracle.f32_to_e4m3(-500.0) == 0xFE
+
+
+def check_quant_rows(qr, rng):
+    x = bf16(rng.standard_normal((7, 96)).astype(np.float32) * rng.random((7, 1)).astype(np.float32))
+    x[3] = 0                                   # an all-zero row keeps scale 1
+    q, s = qr(x)
+    xf = ig.bf16_bits_to_f64(x)
+    for t in range(7):
+        amax = np.float32(np.abs(xf[t]).max())
+        if amax == 0:
+            assert s[t] == 1.0 and not q[t].any()
+            continue
+        assert s[t] == np.float32(amax / np.float32(448.0))
+        inv = np.float32(448.0) / amax
+        want = np.array([oracle.f32_to_e4m3(float(np.float32(a) * inv)) for a in xf[t]])
+        assert np.array_equal(q[t], want)
+        # the largest magnitude maps to 448
+        assert abs(oracle.e4m3_to_f64(int(q[t][np.abs(xf[t]).argmax()]))) == 448.0
+
+
+def test_quant_rows_and_cols():
+    check_quant_rows(oracle.quant_rows, np.random.default_rng(32))
+    rng = np.random.default_rng(33)
+    W = bf16(rng.standard_normal((3, 40, 24)).astype(np.float32))
+    q, s = oracle.quant_cols(W)
+    # columns of W[e] are the rows of W[e].T
+    for e in range(3):
+        qe, se = oracle.quant_rows(np.ascontiguousarray(W[e].T))
+        assert np.array_equal(q[e], qe) and np.array_equal(s[e], se)
+
+
+def check_gemm_fp8(gemm, rng):
+    T, k, E, D, N = 21, 2, 4, 64, 40
+    topk = np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int32)
+    _, offsets = oracle.route_counts(topk, E)
+    perm, _ = oracle.build_perm(topk, E, offsets)
+    x = bf16(rng.standard_normal((T, D)).astype(np.float32))
+    W = bf16((rng.standard_normal((E, D, N)) / 8).astype(np.float32))
+    xq, sx = oracle.quant_rows(x)
+    wq, sw = oracle.quant_cols(W)
+    out = gemm(xq, sx, perm, offsets, wq, sw, k, np.arange(T * k))
+    deq = np.vectorize(oracle.e4m3_to_f64)
+    xd = deq(xq) * sx[:, None].astype(np.float64)
+    wd = deq(wq) * sw[:, :, None].astype(np.float64)          # [E, N, D]
+    for e in range(E):
+        lo, hi = offsets[e], offsets[e + 1]
+        ref = xd[perm[lo:hi] // k] @ wd[e].T
+        assert np.all(np.abs(out[lo:hi] - ref) <= 1e-12 * (np.abs(xd[perm[lo:hi] // k]) @ np.abs(wd[e]).T))
+    # and it approximates the bf16 GEMM within E4M3's precision
+    bf = oracle.gemm_rows(x, perm, offsets, W, k, np.arange(T * k))
+    assert np.abs(out - bf).max() < 0.2 * np.abs(bf).max()
+
+
+def test_gemm_fp8_pins():
+    check_gemm_fp8(oracle.gemm_fp8_rows, np.random.default_rng(34))
+
+
+def test_planted_fp8_mistakes_are_caught():
+    def scale_swapped(xq, sx, perm, offsets, wq, sw, k, rows):     # W scale by row, x by column
+        out = oracle.gemm_fp8_rows(xq, np.ones_like(sx), perm, offsets, wq, np.ones_like(sw), k, rows)
+        return out * sw.mean() * sx.mean()
+
+    def unscaled_rows(xq):                                          # amax not mapped to 448
+        q, s = oracle.quant_rows(xq)
+        return q, s * 2
+    with pytest.raises(AssertionError):
+        check_gemm_fp8(scale_swapped, np.random.default_rng(34))
+    with pytest.raises(AssertionError):
+        check_quant_rows(unscaled_rows, np.random.default_rng(32))
