@@ -236,7 +236,11 @@ double oracle_e4m3_to_f64(uint8_t c) {
 
 /* One vector quantised with one scale, in float32 arithmetic:
  *   amax = max |v|,  inv = 448 / amax,  code = E4M3(v * inv),
- *   scale = amax / 448   (amax == 0: inv = scale = 1). */
+ *   scale = amax / 448.
+ * When amax == 0, or amax is so small (below 448 / FLT_MAX, about 1.3e-36)
+ * that 448 / amax overflows, inv = scale = 1: every |v| is then far below
+ * E4M3's smallest step and every code is zero, as for an all-zero vector.
+ * Inputs are finite. */
 static void quant_vec(const uint16_t* v, int64_t n, int64_t stride, uint8_t* q, int64_t qstride,
                       float* scale) {
     float amax = 0.0f;
@@ -244,8 +248,10 @@ static void quant_vec(const uint16_t* v, int64_t n, int64_t stride, uint8_t* q, 
         const float a = fabsf((float)oracle_bf16_to_f64(v[i * stride]));
         if (a > amax) amax = a;
     }
-    const float inv = amax > 0.0f ? 448.0f / amax : 1.0f;
-    *scale = amax > 0.0f ? amax / 448.0f : 1.0f;
+    const float r = 448.0f / amax;
+    const int plain = amax > 0.0f && isfinite(r);
+    const float inv = plain ? r : 1.0f;
+    *scale = plain ? amax / 448.0f : 1.0f;
     for (int64_t i = 0; i < n; ++i)
         q[i * qstride] = oracle_f32_to_e4m3((float)oracle_bf16_to_f64(v[i * stride]) * inv);
 }

@@ -389,11 +389,24 @@ def test_e4m3_conversion_against_torch_and_format():
 def check_quant_rows(qr, rng):
     x = bf16(rng.standard_normal((7, 96)).astype(np.float32) * rng.random((7, 1)).astype(np.float32))
     x[3] = 0                                   # an all-zero row keeps scale 1
+    x[5] = 0
+    x[5, 9] = 0x0001                           # amax = 2^-133: 448 / amax overflows float32
+    x[6] = 0
+    x[6, 2] = 0x0C00                           # amax = 2^-103: 448 / amax is finite
     q, s = qr(x)
     xf = ig.bf16_bits_to_f64(x)
+    # every row is reconstructed within E4M3's error: half a step of the
+    # 3-bit mantissa (2^-4 relative) for normal codes, half the subnormal
+    # step 2^-9 (scaled) below 2^-6
+    deq = np.array([[oracle.e4m3_to_f64(int(c)) for c in row] for row in q]) * s[:, None]
+    assert np.all(np.abs(deq - xf) <= 2.0 ** -4 * np.abs(xf) + 2.0 ** -10 * s[:, None].astype(np.float64))
+    assert s[5] == 1.0 and not q[5].any()
+    assert s[6] == np.float32(2.0 ** -103 / 448.0) and q[6, 2] == 0x7E
     for t in range(7):
         amax = np.float32(np.abs(xf[t]).max())
-        if amax == 0:
+        with np.errstate(over="ignore", divide="ignore"):
+            overflow = not np.isfinite(np.float32(448.0) / amax)
+        if overflow:
             assert s[t] == 1.0 and not q[t].any()
             continue
         assert s[t] == np.float32(amax / np.float32(448.0))
