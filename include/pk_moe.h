@@ -131,6 +131,56 @@ int pk_moe_dispatch_gemm(const uint16_t* x, const int32_t* perm, const int32_t* 
                          int32_t D_expert, uint16_t* out, int32_t* status_word, void* stream);
 
 /*
+ * FP8 variant of the dispatch GEMM ("ThunderKittens 2.0 & FP8/NVFP4": FP8
+ * tensor-core primitives on Blackwell; the pages fix no scaling granularity,
+ * so this takes one fp32 scale per token row of x and one per output column
+ * of each W_e). With codes from pk_moe_quant_rows / pk_moe_quant_weights:
+ *   out[j, n] = bf16_rne( (sum_d E4M3(xq[t, d]) * E4M3(wq[e, n, d])) * sx[t] * sw[e, n] )
+ *   for t = perm[j] / k, j in expert e's segment; the sum runs on the tensor
+ *   cores (tcgen05.mma kind::f8f6f4) with fp32 accumulation, the two scale
+ *   multiplications in fp32, in that order.
+ *   xq       device uint8 E4M3 codes [T, D], 16-byte aligned
+ *   sx       device fp32 [T]
+ *   perm     device int32 [T*k]; expert_offsets device int32 [E + 1]
+ *   wq       device uint8 E4M3 codes [E, D_expert, D] (each output column's D
+ *            codes contiguous), 16-byte aligned
+ *   sw       device fp32 [E, D_expert], 16-byte aligned
+ *   out      device bf16 [T*k, D_expert], 16-byte aligned
+ * Requires D a multiple of 16, D_expert a multiple of 8; otherwise as
+ * pk_moe_dispatch_gemm (clamped offsets, PK_ERR_BAD_INDEX for a perm entry
+ * outside [0, T*k), whose row then gets scale 0).
+ */
+int pk_moe_dispatch_gemm_fp8(const uint8_t* xq, const float* sx, const int32_t* perm,
+                             const int32_t* expert_offsets, const uint8_t* wq, const float* sw,
+                             int32_t T, int32_t k, int32_t D, int32_t E, int32_t D_expert,
+                             uint16_t* out, int32_t* status_word, void* stream);
+
+/*
+ * E4M3 quantisation of the activations, one fp32 scale per row: with
+ * a = max_d |x[t, d]| (bf16 values),
+ *   sx[t]     = a / 448                      (1 if a == 0)
+ *   xq[t, d]  = E4M3_rne_satfinite(x[t, d] * (448 / a))   (x[t, d] * 1 if a == 0)
+ * every operation in IEEE fp32 with round-to-nearest-even, so the codes are
+ * a pure function of x. 448 is the largest finite E4M3 value.
+ *   x   device bf16 [T, D], 16-byte aligned; xq device uint8 [T, D], 8-byte
+ *   aligned; sx device fp32 [T]. Requires D a multiple of 8.
+ */
+int pk_moe_quant_rows(const uint16_t* x, int32_t T, int32_t D, uint8_t* xq, float* sx,
+                      void* stream);
+
+/*
+ * E4M3 quantisation of the expert weights, one fp32 scale per (expert,
+ * output column), stored transposed for the FP8 GEMM: with
+ * a = max_d |W[e, d, n]|,
+ *   sw[e, n]     = a / 448                   (1 if a == 0)
+ *   wq[e, n, d]  = E4M3_rne_satfinite(W[e, d, n] * (448 / a))
+ * in IEEE fp32 as above. Done once per weight set.
+ *   W   device bf16 [E, D, N]; wq device uint8 [E, N, D]; sw device fp32 [E, N].
+ */
+int pk_moe_quant_weights(const uint16_t* W, int32_t E, int32_t D, int32_t N, uint8_t* wq,
+                         float* sw, void* stream);
+
+/*
  * Grouped GEMM of rows already in expert order -- the expert MLP's
  * down-projection that follows the up-projection above (same expert
  * segments; "Key claims", Fig. 17 gives D=7168, D_expert=2048): for every

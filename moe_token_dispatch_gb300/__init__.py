@@ -25,7 +25,10 @@ from ._binding import (  # noqa: F401
     pk_moe_build_perm,
     pk_moe_combine,
     pk_moe_dispatch_gemm,
+    pk_moe_dispatch_gemm_fp8,
     pk_moe_grouped_gemm,
+    pk_moe_quant_rows,
+    pk_moe_quant_weights,
     pk_moe_route_counts,
     pk_moe_route_noalloc,
     pk_moe_router_topk,

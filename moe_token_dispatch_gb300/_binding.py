@@ -53,6 +53,12 @@ def _load():
     lib.pk_moe_route_noalloc.argtypes = [P, I32, I32, I32, P, P, P, P, P, P]
     lib.pk_moe_grouped_gemm.restype = ctypes.c_int
     lib.pk_moe_grouped_gemm.argtypes = [P, P, P, I32, I32, I32, I32, P, P, P]
+    lib.pk_moe_dispatch_gemm_fp8.restype = ctypes.c_int
+    lib.pk_moe_dispatch_gemm_fp8.argtypes = [P, P, P, P, P, P, I32, I32, I32, I32, I32, P, P, P]
+    lib.pk_moe_quant_rows.restype = ctypes.c_int
+    lib.pk_moe_quant_rows.argtypes = [P, I32, I32, P, P, P]
+    lib.pk_moe_quant_weights.restype = ctypes.c_int
+    lib.pk_moe_quant_weights.argtypes = [P, I32, I32, I32, P, P, P]
     lib.pk_moe_router_topk.restype = ctypes.c_int
     lib.pk_moe_router_topk.argtypes = [P, I32, I32, I32, P, P, P]
     lib.pk_moe_combine.restype = ctypes.c_int
@@ -173,6 +179,43 @@ def pk_moe_grouped_gemm(A: torch.Tensor, expert_offsets: torch.Tensor, W: torch.
                                  _ptr(out, torch.bfloat16, "out", R * N),
                                  _ptr(status_word, torch.int32, "status_word", 1), _stream(stream))
     _check(rc, "pk_moe_grouped_gemm")
+
+
+def pk_moe_dispatch_gemm_fp8(xq: torch.Tensor, sx: torch.Tensor, perm: torch.Tensor,
+                             expert_offsets: torch.Tensor, wq: torch.Tensor, sw: torch.Tensor,
+                             k: int, out: torch.Tensor, status_word: torch.Tensor | None = None,
+                             stream=None) -> None:
+    """xq: uint8 E4M3 codes [T, D]; wq: uint8 codes [E, D_expert, D]."""
+    T, D = xq.shape
+    E, De, D2 = wq.shape
+    if D2 != D:
+        raise ValueError(f"wq is [E, De, {D2}] but xq has D={D}")
+    rc = lib.pk_moe_dispatch_gemm_fp8(
+        _ptr(xq, torch.uint8, "xq"), _ptr(sx, torch.float32, "sx", T),
+        _ptr(perm, torch.int32, "perm", T * k),
+        _ptr(expert_offsets, torch.int32, "expert_offsets", E + 1),
+        _ptr(wq, torch.uint8, "wq"), _ptr(sw, torch.float32, "sw", E * De), T, k, D, E, De,
+        _ptr(out, torch.bfloat16, "out", T * k * De),
+        _ptr(status_word, torch.int32, "status_word", 1), _stream(stream))
+    _check(rc, "pk_moe_dispatch_gemm_fp8")
+
+
+def pk_moe_quant_rows(x: torch.Tensor, xq: torch.Tensor, sx: torch.Tensor, stream=None) -> None:
+    T, D = x.shape
+    rc = lib.pk_moe_quant_rows(_ptr(x, torch.bfloat16, "x"), T, D,
+                               _ptr(xq, torch.uint8, "xq", T * D),
+                               _ptr(sx, torch.float32, "sx", T), _stream(stream))
+    _check(rc, "pk_moe_quant_rows")
+
+
+def pk_moe_quant_weights(W: torch.Tensor, wq: torch.Tensor, sw: torch.Tensor,
+                         stream=None) -> None:
+    """W: bf16 [E, D, N] -> wq uint8 [E, N, D], sw fp32 [E, N]."""
+    E, D, N = W.shape
+    rc = lib.pk_moe_quant_weights(_ptr(W, torch.bfloat16, "W"), E, D, N,
+                                  _ptr(wq, torch.uint8, "wq", E * N * D),
+                                  _ptr(sw, torch.float32, "sw", E * N), _stream(stream))
+    _check(rc, "pk_moe_quant_weights")
 
 
 def pk_moe_router_topk(logits: torch.Tensor, k: int, topk_idx: torch.Tensor,

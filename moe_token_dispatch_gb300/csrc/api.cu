@@ -89,6 +89,44 @@ int pk_moe_dispatch_gemm(const uint16_t* x, const int32_t* perm, const int32_t* 
                                     g_wait_limit_ns.load(std::memory_order_relaxed));
 }
 
+int pk_moe_dispatch_gemm_fp8(const uint8_t* xq, const float* sx, const int32_t* perm,
+                             const int32_t* expert_offsets, const uint8_t* wq, const float* sw,
+                             int32_t T, int32_t k, int32_t D, int32_t E, int32_t D_expert,
+                             uint16_t* out, int32_t* status_word, void* stream) {
+    if (T < 0 || k < 1 || E < 1 || D < 1 || D_expert < 1) return PK_ERR_INVALID_ARG;
+    if ((D % 16) != 0 || (D_expert % 8) != 0) return PK_ERR_INVALID_ARG;
+    const int64_t R = static_cast<int64_t>(T) * k;
+    if (R >= (int64_t{1} << 31)) return PK_ERR_UNSUPPORTED;
+    if (R == 0) return PK_OK;
+    if (!xq || !sx || !perm || !expert_offsets || !wq || !sw || !out) return PK_ERR_INVALID_ARG;
+    if (!aligned16(xq) || !aligned16(wq) || !aligned16(sw) || !aligned16(out))
+        return PK_ERR_INVALID_ARG;
+    return pk::launch_dispatch_gemm_fp8(xq, sx, perm, expert_offsets, wq, sw, T, k, D, E,
+                                        D_expert, out, status_word,
+                                        static_cast<cudaStream_t>(stream),
+                                        g_wait_limit_ns.load(std::memory_order_relaxed));
+}
+
+int pk_moe_quant_rows(const uint16_t* x, int32_t T, int32_t D, uint8_t* xq, float* sx,
+                      void* stream) {
+    if (T < 0 || D < 1 || (D % 8) != 0) return PK_ERR_INVALID_ARG;
+    if (T == 0) return PK_OK;
+    if (!x || !xq || !sx) return PK_ERR_INVALID_ARG;
+    if (!aligned16(x) || (reinterpret_cast<uintptr_t>(xq) & 7u) != 0) return PK_ERR_INVALID_ARG;
+    cudaError_t err = pk::launch_quant_rows(x, T, D, xq, sx, static_cast<cudaStream_t>(stream));
+    return err == cudaSuccess ? PK_OK : PK_ERR_CUDA;
+}
+
+int pk_moe_quant_weights(const uint16_t* W, int32_t E, int32_t D, int32_t N, uint8_t* wq,
+                         float* sw, void* stream) {
+    if (E < 1 || D < 1 || N < 1) return PK_ERR_INVALID_ARG;
+    if (E > 65535) return PK_ERR_UNSUPPORTED;  // experts are a grid dimension
+    if (!W || !wq || !sw) return PK_ERR_INVALID_ARG;
+    cudaError_t err =
+        pk::launch_quant_cols(W, E, D, N, wq, sw, static_cast<cudaStream_t>(stream));
+    return err == cudaSuccess ? PK_OK : PK_ERR_CUDA;
+}
+
 int pk_moe_grouped_gemm(const uint16_t* A, const int32_t* expert_offsets, const uint16_t* W,
                         int32_t R, int32_t K, int32_t N, int32_t E, uint16_t* out,
                         int32_t* status_word, void* stream) {

@@ -34,6 +34,13 @@
 // expert MLP: out2[j, :] = h[j, :] @ W2[e(j)]): the W producer then also
 // TMA-loads each m-tile of A as one 128-row box, and the gather warps idle.
 //
+// With kFp8, the same pipeline is the FP8 variant of the expert GEMM: x and W
+// arrive as E4M3 codes with one fp32 scale per token row and per (expert,
+// output column); a stage then holds K = 128 codes (still 128 bytes per row),
+// W is read K-major ([E, N, D] codes: each output column's codes contiguous),
+// the MMAs are tcgen05.mma kind::f8f6f4 with K = 32, and the epilogue
+// multiplies each accumulator by its row's and column's scale.
+//
 // Work unit = (expert e, group of m-tiles, n-tile), with a shape chosen per
 // expert so that TMEM (512 fp32 columns x 128 lanes) holds every accumulator
 // of the unit and each W tile is loaded once per unit:
@@ -64,8 +71,9 @@ namespace dg {
 
 constexpr int BM = 128;                      // rows per m-tile (MMA M)
 constexpr int BK = 64;                       // K per stage: one 128-byte swizzle row of bf16
-constexpr int B_BOX = 64;                    // W box: 64 columns x 64 rows
-constexpr int B_BOX_BYTES = B_BOX * BK * 2;  // 8 KiB
+constexpr int ROW_BYTES = 128;               // bytes of one row segment per stage (either type)
+constexpr int B_BOX = 64;                    // W box: 64 columns (bf16) or 64 rows (FP8 codes)
+constexpr int B_BOX_BYTES = B_BOX * ROW_BYTES;  // 8 KiB
 constexpr int A_BYTES = BM * BK * 2;         // 16 KiB per m-tile
 constexpr int STAGES = 3;
 constexpr int STAGE_BYTES = 64 * 1024;       // W tile (bn_max*128 B) + m-tiles
@@ -198,10 +206,29 @@ __device__ __forceinline__ void store_row_chunk(uint16_t* dst, const uint32_t (&
     }
 }
 
-template <bool kGather>
+// FP8 epilogue: accumulator x row scale x column scale (fp32), then bf16.
+__device__ __forceinline__ void store_row_chunk_scaled(uint16_t* dst, uint32_t (&v)[32], int col0,
+                                                       int De, float rs,
+                                                       const float* __restrict__ sw_e) {
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+        if (col0 + g * 8 < De) {
+            const float4 s0 = __ldg(reinterpret_cast<const float4*>(sw_e + col0 + g * 8));
+            const float4 s1 = __ldg(reinterpret_cast<const float4*>(sw_e + col0 + g * 8 + 4));
+            const float sc[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+#pragma unroll
+            for (int h = 0; h < 8; ++h)
+                v[g * 8 + h] = __float_as_uint(__uint_as_float(v[g * 8 + h]) * rs * sc[h]);
+        }
+    }
+    store_row_chunk(dst, v, col0, De);
+}
+
+template <bool kGather, bool kFp8>
 __global__ void __launch_bounds__(THREADS, 1)
     k_dispatch_gemm(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap amap,
-                    const uint16_t* __restrict__ x,
+                    const uint8_t* __restrict__ x, const float* __restrict__ sx,
+                    const float* __restrict__ sw,
                     const int32_t* __restrict__ perm, const int32_t* __restrict__ offsets,
                     uint16_t* __restrict__ out, int32_t T, int32_t k, int32_t D, int32_t E,
                     int32_t De, int32_t* status, uint64_t limit) {
@@ -213,7 +240,10 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int R = T * k;
-    const int nk = (D + BK - 1) / BK;
+    constexpr int ELEM = kFp8 ? 1 : 2;              // bytes per element
+    constexpr int BKE = ROW_BYTES / ELEM;           // K elements per stage
+    constexpr int KCHUNK = 16 / ELEM;               // K elements per 16-byte chunk
+    const int nk = (D + BKE - 1) / BKE;
 
     const uint32_t full0 = smem_addr(&ctl->full[0]);
     const uint32_t empty0 = smem_addr(&ctl->empty[0]);
@@ -276,12 +306,12 @@ __global__ void __launch_bounds__(THREADS, 1)
                             bad = true;
                             f = 0;
                         }
-                        p = reinterpret_cast<const char*>(x + static_cast<int64_t>(f / k) * D) +
+                        p = reinterpret_cast<const char*>(x + static_cast<int64_t>(f / k) * D * ELEM) +
                             c * 16;
                     }
                     src[mt][i] = p;
                 }
-            const uint32_t a_off = static_cast<uint32_t>(U.bn_max) * (BK * 2);
+            const uint32_t a_off = static_cast<uint32_t>(U.bn_max) * ROW_BYTES;
             for (int ks = 0; ks < nk; ++ks) {
                 if (!warp_wait(empty0 + 8 * stage, phase ^ 1u, abort, limit)) {
                     if (lane == 0) fail(abort, status);
@@ -289,8 +319,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                     break;
                 }
                 const uint32_t dst0 = sbase + stage * STAGE_BYTES + a_off + rb * 128 + swz;
-                const uint32_t nbytes = (ks * BK + c * 8 < D) ? 16u : 0u;
-                const int64_t koff = static_cast<int64_t>(ks) * BK * 2;
+                const uint32_t nbytes = (ks * BKE + c * KCHUNK < D) ? 16u : 0u;
+                const int64_t koff = static_cast<int64_t>(ks) * ROW_BYTES;
 #pragma unroll
                 for (int mt = 0; mt < MAX_MPU; ++mt)
 #pragma unroll
@@ -323,8 +353,12 @@ __global__ void __launch_bounds__(THREADS, 1)
             bool pf_live = pf.find(pf_u, PU);
             auto prefetch_one = [&]() {
                 if (!pf_live) return;
-                for (int b = 0; b < PU.bn / B_BOX; ++b)
-                    tma_prefetch_3d(&wmap, PU.n0 + b * B_BOX, pf_ks * BK, PU.e);
+                for (int b = 0; b < PU.bn / B_BOX; ++b) {
+                    if (kFp8)
+                        tma_prefetch_3d(&wmap, pf_ks * BKE, PU.n0 + b * B_BOX, PU.e);
+                    else
+                        tma_prefetch_3d(&wmap, PU.n0 + b * B_BOX, pf_ks * BKE, PU.e);
+                }
                 if (++pf_ks == nk) {
                     pf_ks = 0;
                     pf_u += gridDim.x;
@@ -340,7 +374,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 if (!wk.find(u, U)) break;
                 const int nbox = U.bn / B_BOX;
                 const uint64_t pol = U.shared_w ? pol_reuse : pol_once;
-                const uint32_t a_off = static_cast<uint32_t>(U.bn_max) * (BK * 2);
+                const uint32_t a_off = static_cast<uint32_t>(U.bn_max) * ROW_BYTES;
                 const uint32_t tx = static_cast<uint32_t>(nbox * B_BOX_BYTES) +
                                     (kGather ? 0u : static_cast<uint32_t>(U.mpu * A_BYTES));
                 for (int ks = 0; ks < nk; ++ks) {
@@ -353,12 +387,19 @@ __global__ void __launch_bounds__(THREADS, 1)
                     const uint32_t full = full0 + 8 * stage;
                     mbar_arrive_expect_tx(full, tx);
                     const uint32_t sb = sbase + stage * STAGE_BYTES;
-                    for (int b = 0; b < nbox; ++b)
-                        tma_load_3d(sb + b * B_BOX_BYTES, &wmap, U.n0 + b * B_BOX, ks * BK, U.e,
-                                    full, pol);
+                    for (int b = 0; b < nbox; ++b) {
+                        // bf16: 64 columns x 64 K rows (MN-major); FP8: 128 K codes x 64
+                        // columns (K-major). Either way box b lands 8 KiB further.
+                        if (kFp8)
+                            tma_load_3d(sb + b * B_BOX_BYTES, &wmap, ks * BKE, U.n0 + b * B_BOX,
+                                        U.e, full, pol);
+                        else
+                            tma_load_3d(sb + b * B_BOX_BYTES, &wmap, U.n0 + b * B_BOX, ks * BKE,
+                                        U.e, full, pol);
+                    }
                     if (!kGather)  // rows past the expert's end are loaded but never stored
                         for (int mt = 0; mt < U.mpu; ++mt)
-                            tma_load_2d(sb + a_off + mt * A_BYTES, &amap, ks * BK, U.row0 + mt * BM,
+                            tma_load_2d(sb + a_off + mt * A_BYTES, &amap, ks * BKE, U.row0 + mt * BM,
                                         full, pol_reuse);
                     issued |= 1u << stage;
                     issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
@@ -390,16 +431,21 @@ __global__ void __launch_bounds__(THREADS, 1)
                     break;
                 }
                 tc_fence_after_sync();
-                const uint32_t idesc = idesc_bf16_f32(BM, U.bn, true);
+                const uint32_t idesc =
+                    kFp8 ? idesc_e4m3_f32(BM, U.bn) : idesc_bf16_f32(BM, U.bn, true);
                 // Descriptors of stage 0; a stage adds STAGE_BYTES, an m-tile
                 // A_BYTES, a K step of 16 adds 32 B (A, inside the swizzled
                 // row) or 16 rows = 2 KiB (B). The address field holds bytes >> 4.
                 // A: K-major, rows 128 B apart, 8-row groups 1024 B apart.
                 // B: MN-major (W rows are N-contiguous), 64-column blocks
                 // 8 KiB apart (LBO), 8-row K groups 1024 B apart (SBO).
+                // FP8: B is K-major like A (rows 128 B apart, 8-row groups 1024 B
+                // apart) and a K step of 32 codes moves 32 B inside the row.
                 const uint64_t a_desc0 =
-                    sdesc_sw128(sbase + static_cast<uint32_t>(U.bn_max) * (BK * 2), 16, 1024);
-                const uint64_t b_desc0 = sdesc_sw128(sbase, B_BOX_BYTES, 1024);
+                    sdesc_sw128(sbase + static_cast<uint32_t>(U.bn_max) * ROW_BYTES, 16, 1024);
+                const uint64_t b_desc0 = kFp8 ? sdesc_sw128(sbase, 16, 1024)
+                                              : sdesc_sw128(sbase, B_BOX_BYTES, 1024);
+                constexpr uint32_t b_step = kFp8 ? (32 >> 4) : ((UMMA_K * 128) >> 4);
                 const int mpu = U.mpu;
                 const uint32_t acc_stride = static_cast<uint32_t>(U.bn_max);
                 for (int ks = 0; ks < nk; ++ks) {
@@ -418,10 +464,14 @@ __global__ void __launch_bounds__(THREADS, 1)
                         const uint64_t a_mt = a_st + static_cast<uint64_t>(mt) * (A_BYTES >> 4);
                         const uint32_t d = tmem + static_cast<uint32_t>(mt) * acc_stride;
 #pragma unroll
-                        for (int kk = 0; kk < BK / UMMA_K; ++kk)
-                            mma_bf16(d, a_mt + kk * ((UMMA_K * 2) >> 4),
-                                     b_st + kk * ((UMMA_K * 128) >> 4), idesc,
-                                     (ks | kk) != 0 ? 1u : 0u);
+                        for (int kk = 0; kk < 4; ++kk) {  // four K steps of 32 bytes per stage
+                            if (kFp8)
+                                mma_f8(d, a_mt + kk * (32 >> 4), b_st + kk * b_step, idesc,
+                                       (ks | kk) != 0 ? 1u : 0u);
+                            else
+                                mma_bf16(d, a_mt + kk * (32 >> 4), b_st + kk * b_step, idesc,
+                                         (ks | kk) != 0 ? 1u : 0u);
+                        }
                     }
                     mma_commit(empty0 + 8 * stage);
                     if (++stage == STAGES) {
@@ -464,6 +514,12 @@ __global__ void __launch_bounds__(THREADS, 1)
                 const int r = rbase + lane;
                 const bool valid = r < U.rows;
                 uint16_t* orow = out + static_cast<int64_t>(U.row0 + r) * De;
+                float rs = 1.0f;  // FP8: this row's token scale
+                if (kFp8 && valid) {
+                    const int f = __ldg(perm + U.row0 + r);
+                    rs = (f >= 0 && f < R) ? __ldg(sx + f / k) : 0.0f;
+                }
+                const float* sw_e = kFp8 ? sw + static_cast<int64_t>(U.e) * De : nullptr;
                 const uint32_t tbase = tmem + (static_cast<uint32_t>(q * 32) << 16) +
                                        static_cast<uint32_t>(mt * U.bn_max);
                 for (int cc = 0; cc < U.bn / 32; cc += 2) {
@@ -478,8 +534,13 @@ __global__ void __launch_bounds__(THREADS, 1)
                         released = true;
                     }
                     if (valid) {
-                        store_row_chunk(orow, v0, U.n0 + cc * 32, De);
-                        store_row_chunk(orow, v1, U.n0 + cc * 32 + 32, De);
+                        if (kFp8) {
+                            store_row_chunk_scaled(orow, v0, U.n0 + cc * 32, De, rs, sw_e);
+                            store_row_chunk_scaled(orow, v1, U.n0 + cc * 32 + 32, De, rs, sw_e);
+                        } else {
+                            store_row_chunk(orow, v0, U.n0 + cc * 32, De);
+                            store_row_chunk(orow, v1, U.n0 + cc * 32 + 32, De);
+                        }
                     }
                 }
             }
@@ -534,9 +595,11 @@ namespace {
 
 // Builds the tensor maps and launches one instantiation. A is x (gathered
 // through perm) or, without gather, the [T, D] matrix of expert-sorted rows.
-int launch_common(bool gather, const uint16_t* A, const int32_t* perm, const int32_t* offsets,
-                  const uint16_t* W, int32_t T, int32_t k, int32_t D, int32_t E, int32_t De,
-                  uint16_t* out, int32_t* status, cudaStream_t stream, uint64_t wait_limit_ns) {
+// fp8: x and W are E4M3 codes (W as [E, De, D]) with scales sx [T], sw [E, De].
+int launch_common(bool gather, bool fp8, const void* A, const float* sx, const int32_t* perm,
+                  const int32_t* offsets, const void* W, const float* sw, int32_t T, int32_t k,
+                  int32_t D, int32_t E, int32_t De, uint16_t* out, int32_t* status,
+                  cudaStream_t stream, uint64_t wait_limit_ns) {
     using namespace dg;
     auto enc = encoder();
     if (!enc) return PK_ERR_CUDA;
@@ -549,10 +612,13 @@ int launch_common(bool gather, const uint16_t* A, const int32_t* perm, const int
         if (!di.attr_set) {
             if (cudaDeviceGetAttribute(&di.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
                 return PK_ERR_CUDA;
-            if (cudaFuncSetAttribute(k_dispatch_gemm<true>,
+            if (cudaFuncSetAttribute(k_dispatch_gemm<true, false>,
                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      SMEM_BYTES) != cudaSuccess ||
-                cudaFuncSetAttribute(k_dispatch_gemm<false>,
+                cudaFuncSetAttribute(k_dispatch_gemm<false, false>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     SMEM_BYTES) != cudaSuccess ||
+                cudaFuncSetAttribute(k_dispatch_gemm<true, true>,
                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      SMEM_BYTES) != cudaSuccess)
                 return PK_ERR_CUDA;
@@ -562,14 +628,26 @@ int launch_common(bool gather, const uint16_t* A, const int32_t* perm, const int
     }
 
     CUtensorMap wmap, amap;
-    {
+    if (fp8) {
+        // W codes [E, De, D]: boxes of 128 K codes x 64 output columns, 128-byte swizzle
+        cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(De),
+                              static_cast<cuuint64_t>(E)};
+        cuuint64_t strides[2] = {static_cast<cuuint64_t>(D),
+                                 static_cast<cuuint64_t>(D) * static_cast<cuuint64_t>(De)};
+        cuuint32_t box[3] = {ROW_BYTES, B_BOX, 1};
+        cuuint32_t es[3] = {1, 1, 1};
+        if (enc(&wmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(W), dims, strides, box,
+                es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return PK_ERR_UNSUPPORTED;
+    } else {
         cuuint64_t dims[3] = {static_cast<cuuint64_t>(De), static_cast<cuuint64_t>(D),
                               static_cast<cuuint64_t>(E)};
         cuuint64_t strides[2] = {static_cast<cuuint64_t>(De) * 2,
                                  static_cast<cuuint64_t>(D) * static_cast<cuuint64_t>(De) * 2};
         cuuint32_t box[3] = {B_BOX, BK, 1};
         cuuint32_t es[3] = {1, 1, 1};
-        if (enc(&wmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<uint16_t*>(W), dims, strides,
+        if (enc(&wmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(W), dims, strides,
                 box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return PK_ERR_UNSUPPORTED;
@@ -582,17 +660,23 @@ int launch_common(bool gather, const uint16_t* A, const int32_t* perm, const int
         cuuint64_t strides[1] = {static_cast<cuuint64_t>(D) * 2};
         cuuint32_t box[2] = {BK, BM};
         cuuint32_t es[2] = {1, 1};
-        if (enc(&amap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(A), dims, strides,
+        if (enc(&amap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(A), dims, strides,
                 box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return PK_ERR_UNSUPPORTED;
     }
-    if (gather)
-        k_dispatch_gemm<true><<<sms, THREADS, SMEM_BYTES, stream>>>(
-            wmap, amap, A, perm, offsets, out, T, k, D, E, De, status, wait_limit_ns);
+    const uint8_t* a8 = static_cast<const uint8_t*>(A);
+    if (fp8)
+        k_dispatch_gemm<true, true><<<sms, THREADS, SMEM_BYTES, stream>>>(
+            wmap, amap, a8, sx, sw, perm, offsets, out, T, k, D, E, De, status, wait_limit_ns);
+    else if (gather)
+        k_dispatch_gemm<true, false><<<sms, THREADS, SMEM_BYTES, stream>>>(
+            wmap, amap, a8, nullptr, nullptr, perm, offsets, out, T, k, D, E, De, status,
+            wait_limit_ns);
     else
-        k_dispatch_gemm<false><<<sms, THREADS, SMEM_BYTES, stream>>>(
-            wmap, amap, A, perm, offsets, out, T, k, D, E, De, status, wait_limit_ns);
+        k_dispatch_gemm<false, false><<<sms, THREADS, SMEM_BYTES, stream>>>(
+            wmap, amap, a8, nullptr, nullptr, perm, offsets, out, T, k, D, E, De, status,
+            wait_limit_ns);
     return cudaGetLastError() == cudaSuccess ? PK_OK : PK_ERR_CUDA;
 }
 
@@ -602,15 +686,24 @@ int launch_dispatch_gemm(const uint16_t* x, const int32_t* perm, const int32_t* 
                          const uint16_t* W, int32_t T, int32_t k, int32_t D, int32_t E,
                          int32_t De, uint16_t* out, int32_t* status, cudaStream_t stream,
                          uint64_t wait_limit_ns) {
-    return launch_common(true, x, perm, offsets, W, T, k, D, E, De, out, status, stream,
-                         wait_limit_ns);
+    return launch_common(true, false, x, nullptr, perm, offsets, W, nullptr, T, k, D, E, De, out,
+                         status, stream, wait_limit_ns);
+}
+
+int launch_dispatch_gemm_fp8(const uint8_t* xq, const float* sx, const int32_t* perm,
+                             const int32_t* offsets, const uint8_t* wq, const float* sw,
+                             int32_t T, int32_t k, int32_t D, int32_t E, int32_t De,
+                             uint16_t* out, int32_t* status, cudaStream_t stream,
+                             uint64_t wait_limit_ns) {
+    return launch_common(true, true, xq, sx, perm, offsets, wq, sw, T, k, D, E, De, out, status,
+                         stream, wait_limit_ns);
 }
 
 int launch_grouped_gemm(const uint16_t* A, const int32_t* offsets, const uint16_t* W, int32_t R,
                         int32_t K, int32_t N, int32_t E, uint16_t* out, int32_t* status,
                         cudaStream_t stream, uint64_t wait_limit_ns) {
-    return launch_common(false, A, nullptr, offsets, W, R, 1, K, E, N, out, status, stream,
-                         wait_limit_ns);
+    return launch_common(false, false, A, nullptr, nullptr, offsets, W, nullptr, R, 1, K, E, N,
+                         out, status, stream, wait_limit_ns);
 }
 
 // ------------------------------------------------- bounded-wait check kernel

@@ -28,6 +28,20 @@ int launch_dispatch_gemm(const uint16_t* x, const int32_t* perm, const int32_t* 
                          int32_t De, uint16_t* out, int32_t* status, cudaStream_t stream,
                          uint64_t wait_limit_ns);
 
+// FP8 dispatch GEMM: E4M3 codes xq [T, D] and wq [E, De, D] with fp32 scales
+// sx [T] and sw [E, De].
+int launch_dispatch_gemm_fp8(const uint8_t* xq, const float* sx, const int32_t* perm,
+                             const int32_t* offsets, const uint8_t* wq, const float* sw,
+                             int32_t T, int32_t k, int32_t D, int32_t E, int32_t De,
+                             uint16_t* out, int32_t* status, cudaStream_t stream,
+                             uint64_t wait_limit_ns);
+
+// E4M3 quantisation with one scale per row of x / per (expert, column) of W.
+cudaError_t launch_quant_rows(const uint16_t* x, int32_t T, int32_t D, uint8_t* q, float* scale,
+                              cudaStream_t stream);
+cudaError_t launch_quant_cols(const uint16_t* W, int32_t E, int32_t D, int32_t N, uint8_t* q,
+                              float* scale, cudaStream_t stream);
+
 // Grouped GEMM of expert-sorted rows (no gather).
 int launch_grouped_gemm(const uint16_t* A, const int32_t* offsets, const uint16_t* W, int32_t R,
                         int32_t K, int32_t N, int32_t E, uint16_t* out, int32_t* status,

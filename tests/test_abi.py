@@ -103,3 +103,28 @@ def test_build_perm_rejects(lib):
     assert _raw(lib).pk_moe_build_perm(FAKE, 4, 2, 8, FAKE, FAKE, None, FAKE, 8, None,
                                        None) == 1
     assert _raw(lib).pk_debug_bounded_wait(None, 10, None) == 1
+
+
+@pytest.mark.parametrize("args,code", [
+    # xq, sx, perm, offsets, wq, sw, T, k, D, E, De, out, status, stream
+    ((FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4, 2, 56, 8, 64, FAKE, None, None), 1),   # D % 16
+    ((FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4, 2, 64, 8, 12, FAKE, None, None), 1),   # De % 8
+    ((FAKE_ODD, FAKE, FAKE, FAKE, FAKE, FAKE, 4, 2, 64, 8, 64, FAKE, None, None), 1),  # xq
+    ((FAKE, FAKE, FAKE, FAKE, FAKE_ODD, FAKE, 4, 2, 64, 8, 64, FAKE, None, None), 1),  # wq
+    ((FAKE, FAKE, FAKE, FAKE, FAKE, FAKE_ODD, 4, 2, 64, 8, 64, FAKE, None, None), 1),  # sw
+    ((FAKE, None, FAKE, FAKE, FAKE, FAKE, 4, 2, 64, 8, 64, FAKE, None, None), 1),   # no sx
+    ((FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1 << 29, 8, 64, 8, 64, FAKE, None, None), 2),
+])
+def test_dispatch_gemm_fp8_rejects(lib, args, code):
+    assert _raw(lib).pk_moe_dispatch_gemm_fp8(*args) == code
+
+
+def test_quant_entry_points_reject(lib):
+    L = _raw(lib)
+    assert L.pk_moe_quant_rows(FAKE, 4, 12, FAKE, FAKE, None) == 1        # D % 8
+    assert L.pk_moe_quant_rows(FAKE_ODD, 4, 16, FAKE, FAKE, None) == 1    # x misaligned
+    assert L.pk_moe_quant_rows(None, 0, 16, None, None, None) == 0        # T == 0: no-op
+    assert L.pk_moe_quant_weights(FAKE, 0, 16, 16, FAKE, FAKE, None) == 1
+    assert L.pk_moe_quant_weights(FAKE, 70000, 16, 16, FAKE, FAKE, None) == 2
+    assert L.pk_moe_dispatch_gemm_fp8(None, None, None, None, None, None, 0, 2, 64, 8, 64,
+                                      None, None, None) == 0
