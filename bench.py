@@ -459,7 +459,8 @@ def run_op(args, wl):
         # would at load time. The timed call is the FP8 dispatch GEMM.
         x = dev_bf16(ig.make_x(wl))
         W = dev_bf16(ig.make_W(wl))
-        wq = torch.empty((wl.E, wl.De, wl.D), dtype=torch.uint8, device=dev)
+        wq = torch.empty((pk.pk_moe_fp8_weight_bytes(wl.E, wl.D, wl.De),), dtype=torch.uint8,
+                         device=dev)
         sw = torch.empty((wl.E, wl.De), dtype=torch.float32, device=dev)
         pk.pk_moe_quant_weights(W, wq, sw, stream)
         del W

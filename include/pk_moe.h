@@ -142,11 +142,13 @@ int pk_moe_dispatch_gemm(const uint16_t* x, const int32_t* perm, const int32_t* 
  *   xq       device uint8 E4M3 codes [T, D], 16-byte aligned
  *   sx       device fp32 [T]
  *   perm     device int32 [T*k]; expert_offsets device int32 [E + 1]
- *   wq       device uint8 E4M3 codes [E, D_expert, D] (each output column's D
- *            codes contiguous), 16-byte aligned
+ *   wq       device uint8 E4M3 codes of W in the blocked layout written by
+ *            pk_moe_quant_weights (pk_moe_fp8_weight_bytes bytes), 16-byte
+ *            aligned
  *   sw       device fp32 [E, D_expert], 16-byte aligned
  *   out      device bf16 [T*k, D_expert], 16-byte aligned
- * Requires D a multiple of 16, D_expert a multiple of 8; otherwise as
+ * Requires D a multiple of 16, D_expert a multiple of 8,
+ * pk_moe_fp8_weight_bytes(E, D, D_expert) < 2^38; otherwise as
  * pk_moe_dispatch_gemm (clamped offsets, PK_ERR_BAD_INDEX for a perm entry
  * outside [0, T*k), whose row then gets scale 0).
  */
@@ -170,13 +172,19 @@ int pk_moe_quant_rows(const uint16_t* x, int32_t T, int32_t D, uint8_t* xq, floa
 
 /*
  * E4M3 quantisation of the expert weights, one fp32 scale per (expert,
- * output column), stored transposed for the FP8 GEMM: with
- * a = max_d |W[e, d, n]|,
- *   sw[e, n]     = a / 448                   (1 if a == 0)
- *   wq[e, n, d]  = E4M3_rne_satfinite(W[e, d, n] * (448 / a))
- * in IEEE fp32 as above. Done once per weight set.
- *   W   device bf16 [E, D, N]; wq device uint8 [E, N, D]; sw device fp32 [E, N].
+ * output column), for the FP8 GEMM: with a = max_d |W[e, d, n]|,
+ *   sw[e, n]        = a / 448                (1 if a == 0)
+ *   code(e, n, d)   = E4M3_rne_satfinite(W[e, d, n] * (448 / a))
+ * in IEEE fp32 as above. Done once per weight set. The codes are stored in
+ * a blocked layout of 64-column x 128-code blocks, each 8 KiB block
+ * contiguous so that the GEMM reads it from memory in one piece:
+ *   wq[(((e * NB + n / 64) * KB + d / 128) * 64 + n % 64) * 128 + d % 128]
+ *     = code(e, n, d),  NB = ceil(N / 64), KB = ceil(D / 128),
+ * and every byte of a block past N or D is 0.
+ *   W   device bf16 [E, D, N]; wq device uint8, pk_moe_fp8_weight_bytes(E, D, N)
+ *   bytes; sw device fp32 [E, N].
  */
+size_t pk_moe_fp8_weight_bytes(int32_t E, int32_t D, int32_t N);
 int pk_moe_quant_weights(const uint16_t* W, int32_t E, int32_t D, int32_t N, uint8_t* wq,
                          float* sw, void* stream);
 

@@ -57,6 +57,8 @@ def _load():
     lib.pk_moe_dispatch_gemm_fp8.argtypes = [P, P, P, P, P, P, I32, I32, I32, I32, I32, P, P, P]
     lib.pk_moe_quant_rows.restype = ctypes.c_int
     lib.pk_moe_quant_rows.argtypes = [P, I32, I32, P, P, P]
+    lib.pk_moe_fp8_weight_bytes.restype = SZ
+    lib.pk_moe_fp8_weight_bytes.argtypes = [I32, I32, I32]
     lib.pk_moe_quant_weights.restype = ctypes.c_int
     lib.pk_moe_quant_weights.argtypes = [P, I32, I32, I32, P, P, P]
     lib.pk_moe_router_topk.restype = ctypes.c_int
@@ -185,16 +187,16 @@ def pk_moe_dispatch_gemm_fp8(xq: torch.Tensor, sx: torch.Tensor, perm: torch.Ten
                              expert_offsets: torch.Tensor, wq: torch.Tensor, sw: torch.Tensor,
                              k: int, out: torch.Tensor, status_word: torch.Tensor | None = None,
                              stream=None) -> None:
-    """xq: uint8 E4M3 codes [T, D]; wq: uint8 codes [E, D_expert, D]."""
+    """xq: uint8 E4M3 codes [T, D]; wq: the blocked codes pk_moe_quant_weights
+    writes; sw: fp32 [E, D_expert] (gives E and D_expert)."""
     T, D = xq.shape
-    E, De, D2 = wq.shape
-    if D2 != D:
-        raise ValueError(f"wq is [E, De, {D2}] but xq has D={D}")
+    E, De = sw.shape
     rc = lib.pk_moe_dispatch_gemm_fp8(
         _ptr(xq, torch.uint8, "xq"), _ptr(sx, torch.float32, "sx", T),
         _ptr(perm, torch.int32, "perm", T * k),
         _ptr(expert_offsets, torch.int32, "expert_offsets", E + 1),
-        _ptr(wq, torch.uint8, "wq"), _ptr(sw, torch.float32, "sw", E * De), T, k, D, E, De,
+        _ptr(wq, torch.uint8, "wq", pk_moe_fp8_weight_bytes(E, D, De)),
+        _ptr(sw, torch.float32, "sw", E * De), T, k, D, E, De,
         _ptr(out, torch.bfloat16, "out", T * k * De),
         _ptr(status_word, torch.int32, "status_word", 1), _stream(stream))
     _check(rc, "pk_moe_dispatch_gemm_fp8")
@@ -208,12 +210,17 @@ def pk_moe_quant_rows(x: torch.Tensor, xq: torch.Tensor, sx: torch.Tensor, strea
     _check(rc, "pk_moe_quant_rows")
 
 
+def pk_moe_fp8_weight_bytes(E: int, D: int, N: int) -> int:
+    return int(lib.pk_moe_fp8_weight_bytes(E, D, N))
+
+
 def pk_moe_quant_weights(W: torch.Tensor, wq: torch.Tensor, sw: torch.Tensor,
                          stream=None) -> None:
-    """W: bf16 [E, D, N] -> wq uint8 [E, N, D], sw fp32 [E, N]."""
+    """W: bf16 [E, D, N] -> wq uint8 blocked codes (pk_moe_fp8_weight_bytes
+    bytes), sw fp32 [E, N]."""
     E, D, N = W.shape
     rc = lib.pk_moe_quant_weights(_ptr(W, torch.bfloat16, "W"), E, D, N,
-                                  _ptr(wq, torch.uint8, "wq", E * N * D),
+                                  _ptr(wq, torch.uint8, "wq", pk_moe_fp8_weight_bytes(E, D, N)),
                                   _ptr(sw, torch.float32, "sw", E * N), _stream(stream))
     _check(rc, "pk_moe_quant_weights")
 

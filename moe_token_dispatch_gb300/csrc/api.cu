@@ -101,6 +101,7 @@ int pk_moe_dispatch_gemm_fp8(const uint8_t* xq, const float* sx, const int32_t* 
     if (!xq || !sx || !perm || !expert_offsets || !wq || !sw || !out) return PK_ERR_INVALID_ARG;
     if (!aligned16(xq) || !aligned16(wq) || !aligned16(sw) || !aligned16(out))
         return PK_ERR_INVALID_ARG;
+    if (pk_moe_fp8_weight_bytes(E, D, D_expert) >= (size_t{1} << 38)) return PK_ERR_UNSUPPORTED;
     return pk::launch_dispatch_gemm_fp8(xq, sx, perm, expert_offsets, wq, sw, T, k, D, E,
                                         D_expert, out, status_word,
                                         static_cast<cudaStream_t>(stream),
@@ -115,6 +116,12 @@ int pk_moe_quant_rows(const uint16_t* x, int32_t T, int32_t D, uint8_t* xq, floa
     if (!aligned16(x) || (reinterpret_cast<uintptr_t>(xq) & 7u) != 0) return PK_ERR_INVALID_ARG;
     cudaError_t err = pk::launch_quant_rows(x, T, D, xq, sx, static_cast<cudaStream_t>(stream));
     return err == cudaSuccess ? PK_OK : PK_ERR_CUDA;
+}
+
+size_t pk_moe_fp8_weight_bytes(int32_t E, int32_t D, int32_t N) {
+    if (E < 1 || D < 1 || N < 1) return 0;
+    return static_cast<size_t>(E) * static_cast<size_t>((N + 63) / 64) *
+           static_cast<size_t>((D + 127) / 128) * 8192u;
 }
 
 int pk_moe_quant_weights(const uint16_t* W, int32_t E, int32_t D, int32_t N, uint8_t* wq,

@@ -37,9 +37,10 @@
 // With kFp8, the same pipeline is the FP8 variant of the expert GEMM: x and W
 // arrive as E4M3 codes with one fp32 scale per token row and per (expert,
 // output column); a stage then holds K = 128 codes (still 128 bytes per row),
-// W is read K-major ([E, N, D] codes: each output column's codes contiguous),
-// the MMAs are tcgen05.mma kind::f8f6f4 with K = 32, and the epilogue
-// multiplies each accumulator by its row's and column's scale.
+// W is read K-major from a blocked layout in which each 64-column x 128-code
+// box is one contiguous 8 KiB block (so every TMA box is a single contiguous
+// read from HBM), the MMAs are tcgen05.mma kind::f8f6f4 with K = 32, and the
+// epilogue multiplies each accumulator by its row's and column's scale.
 //
 // Work unit = (expert e, group of m-tiles, n-tile), with a shape chosen per
 // expert so that TMEM (512 fp32 columns x 128 lanes) holds every accumulator
@@ -244,6 +245,12 @@ __global__ void __launch_bounds__(THREADS, 1)
     constexpr int BKE = ROW_BYTES / ELEM;           // K elements per stage
     constexpr int KCHUNK = 16 / ELEM;               // K elements per 16-byte chunk
     const int nk = (D + BKE - 1) / BKE;
+    // FP8 blocked W: box (e, column block nb, K block kb) starts at row
+    // ((e * NB + nb) * nk + kb) * 64 of the [rows, 128] code matrix.
+    const int nb_count = (De + B_BOX - 1) / B_BOX;
+    auto fp8_box_row = [&](int e, int nb, int kb) {
+        return ((e * nb_count + nb) * nk + kb) * B_BOX;
+    };
 
     const uint32_t full0 = smem_addr(&ctl->full[0]);
     const uint32_t empty0 = smem_addr(&ctl->empty[0]);
@@ -355,7 +362,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 if (!pf_live) return;
                 for (int b = 0; b < PU.bn / B_BOX; ++b) {
                     if (kFp8)
-                        tma_prefetch_3d(&wmap, pf_ks * BKE, PU.n0 + b * B_BOX, PU.e);
+                        tma_prefetch_2d(&wmap, 0, fp8_box_row(PU.e, PU.n0 / B_BOX + b, pf_ks));
                     else
                         tma_prefetch_3d(&wmap, PU.n0 + b * B_BOX, pf_ks * BKE, PU.e);
                 }
@@ -391,8 +398,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                         // bf16: 64 columns x 64 K rows (MN-major); FP8: 128 K codes x 64
                         // columns (K-major). Either way box b lands 8 KiB further.
                         if (kFp8)
-                            tma_load_3d(sb + b * B_BOX_BYTES, &wmap, ks * BKE, U.n0 + b * B_BOX,
-                                        U.e, full, pol);
+                            tma_load_2d(sb + b * B_BOX_BYTES, &wmap, 0,
+                                        fp8_box_row(U.e, U.n0 / B_BOX + b, ks), full, pol);
                         else
                             tma_load_3d(sb + b * B_BOX_BYTES, &wmap, U.n0 + b * B_BOX, ks * BKE,
                                         U.e, full, pol);
@@ -595,7 +602,8 @@ namespace {
 
 // Builds the tensor maps and launches one instantiation. A is x (gathered
 // through perm) or, without gather, the [T, D] matrix of expert-sorted rows.
-// fp8: x and W are E4M3 codes (W as [E, De, D]) with scales sx [T], sw [E, De].
+// fp8: x and W are E4M3 codes (W blocked, see pk_moe_fp8_weight_bytes) with
+// scales sx [T], sw [E, De].
 int launch_common(bool gather, bool fp8, const void* A, const float* sx, const int32_t* perm,
                   const int32_t* offsets, const void* W, const float* sw, int32_t T, int32_t k,
                   int32_t D, int32_t E, int32_t De, uint16_t* out, int32_t* status,
@@ -629,14 +637,14 @@ int launch_common(bool gather, bool fp8, const void* A, const float* sx, const i
 
     CUtensorMap wmap, amap;
     if (fp8) {
-        // W codes [E, De, D]: boxes of 128 K codes x 64 output columns, 128-byte swizzle
-        cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(De),
-                              static_cast<cuuint64_t>(E)};
-        cuuint64_t strides[2] = {static_cast<cuuint64_t>(D),
-                                 static_cast<cuuint64_t>(D) * static_cast<cuuint64_t>(De)};
-        cuuint32_t box[3] = {ROW_BYTES, B_BOX, 1};
-        cuuint32_t es[3] = {1, 1, 1};
-        if (enc(&wmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(W), dims, strides, box,
+        // blocked W codes: a [rows, 128] matrix of 64-row boxes, 128-byte swizzle
+        const uint64_t rows = static_cast<uint64_t>(E) * ((De + B_BOX - 1) / B_BOX) *
+                              ((D + ROW_BYTES - 1) / ROW_BYTES) * B_BOX;
+        cuuint64_t dims[2] = {static_cast<cuuint64_t>(ROW_BYTES), static_cast<cuuint64_t>(rows)};
+        cuuint64_t strides[1] = {static_cast<cuuint64_t>(ROW_BYTES)};
+        cuuint32_t box[2] = {ROW_BYTES, B_BOX};
+        cuuint32_t es[2] = {1, 1};
+        if (enc(&wmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(W), dims, strides, box,
                 es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return PK_ERR_UNSUPPORTED;

@@ -9,10 +9,11 @@
 //                       (one warp per row, two passes over the row).
 //   k_col_amax,
 //   k_col_convert,
-//   k_col_scale         weights W [E, D, N] -> codes [E, N, D] (each output
-//                       column's D codes contiguous: the K-major operand the
-//                       tensor cores read) + scales [E, N]; done once per
-//                       weight set, not per step.
+//   k_col_scale         weights W [E, D, N] -> codes in the blocked layout
+//                       the FP8 GEMM reads (each 64-column x 128-code block
+//                       contiguous, K-major inside: column n's codes d of one
+//                       block form one 128-byte row) + scales [E, N]; done
+//                       once per weight set, not per step.
 #include <cuda_fp8.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -87,10 +88,13 @@ __global__ void __launch_bounds__(256)
     amax_out[static_cast<int64_t>(e) * N + n] = amax;
 }
 
-// codes of a 32 (d) x 32 (n) tile, written transposed into q[e, n, d]
+// codes of a 32 (d) x 32 (n) tile, written transposed into the blocked
+// layout: code (e, n, d) at byte ((((e * NB + n / 64) * KB + d / 128) * 64 +
+// n % 64) * 128 + d % 128, NB = ceil(N / 64), KB = ceil(D / 128)
 __global__ void __launch_bounds__(256)
     k_col_convert(const uint16_t* __restrict__ W, int32_t D, int32_t N,
                   const float* __restrict__ amax, uint8_t* __restrict__ q) {
+    const int64_t NB = (N + 63) / 64, KB = (D + 127) / 128;
     __shared__ uint8_t tile[32][33];
     const int e = blockIdx.z;
     const int n0 = blockIdx.x * 32, d0 = blockIdx.y * 32;
@@ -114,7 +118,10 @@ __global__ void __launch_bounds__(256)
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
         const int nn = n0 + ty + 8 * i, d = d0 + tx;
-        if (nn < N && d < D) q[(static_cast<int64_t>(e) * N + nn) * D + d] = tile[tx][ty + 8 * i];
+        if (nn < N && d < D) {
+            const int64_t row = ((e * NB + nn / 64) * KB + d / 128) * 64 + nn % 64;
+            q[row * 128 + d % 128] = tile[tx][ty + 8 * i];
+        }
     }
 }
 
@@ -141,9 +148,13 @@ cudaError_t launch_quant_rows(const uint16_t* x, int32_t T, int32_t D, uint8_t* 
 
 cudaError_t launch_quant_cols(const uint16_t* W, int32_t E, int32_t D, int32_t N, uint8_t* q,
                               float* scale, cudaStream_t stream) {
+    // padding of the blocks past D and N reads as code 0
+    const int64_t bytes = static_cast<int64_t>(E) * ((N + 63) / 64) * ((D + 127) / 128) * 8192;
+    cudaError_t err = cudaMemsetAsync(q, 0, static_cast<size_t>(bytes), stream);
+    if (err != cudaSuccess) return err;
     // scale holds each column's amax until the last kernel turns it into the scale
     k_col_amax<<<dim3((N + 255) / 256, E), 256, 0, stream>>>(W, D, N, scale);
-    cudaError_t err = cudaGetLastError();
+    err = cudaGetLastError();
     if (err != cudaSuccess) return err;
     k_col_convert<<<dim3((N + 31) / 32, (D + 31) / 32, E), 256, 0, stream>>>(W, D, N, scale, q);
     err = cudaGetLastError();

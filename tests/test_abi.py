@@ -128,3 +128,11 @@ def test_quant_entry_points_reject(lib):
     assert L.pk_moe_quant_weights(FAKE, 70000, 16, 16, FAKE, FAKE, None) == 2
     assert L.pk_moe_dispatch_gemm_fp8(None, None, None, None, None, None, 0, 2, 64, 8, 64,
                                       None, None, None) == 0
+
+
+def test_fp8_weight_bytes(lib):
+    L = _raw(lib)
+    # 64-column x 128-code blocks of 8 KiB, padded in both directions
+    assert L.pk_moe_fp8_weight_bytes(256, 7168, 2048) == 256 * 32 * 56 * 8192
+    assert L.pk_moe_fp8_weight_bytes(3, 200, 136) == 3 * 3 * 2 * 8192
+    assert L.pk_moe_fp8_weight_bytes(0, 16, 8) == 0

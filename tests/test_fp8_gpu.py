@@ -22,6 +22,16 @@ def _u8_dev(a):
     return torch.from_numpy(np.ascontiguousarray(a, dtype=np.uint8)).cuda()
 
 
+def to_blocked(q):
+    """Codes [E, N, D] (column n's codes contiguous) into the blocked layout
+    of the C ABI: [E, ceil(N/64), ceil(D/128), 64, 128], zero-padded."""
+    E, N, D = q.shape
+    NB, KB = -(-N // 64), -(-D // 128)
+    p = np.zeros((E, NB * 64, KB * 128), dtype=np.uint8)
+    p[:, :N, :D] = q
+    return np.ascontiguousarray(p.reshape(E, NB, 64, KB, 128).transpose(0, 1, 3, 2, 4))
+
+
 def _gpu_quant_rows(pk, x_u16):
     T, D = x_u16.shape
     xq = torch.empty((T, D), dtype=torch.uint8, device="cuda")
@@ -32,8 +42,10 @@ def _gpu_quant_rows(pk, x_u16):
 
 
 def _gpu_quant_weights(pk, W_dev):
+    """Blocked codes, viewed as [E, ceil(N/64), ceil(D/128), 64, 128]."""
     E, D, N = W_dev.shape
-    wq = torch.empty((E, N, D), dtype=torch.uint8, device="cuda")
+    wq = torch.full((E, -(-N // 64), -(-D // 128), 64, 128), 0x55, dtype=torch.uint8,
+                    device="cuda")  # padding must come back zero
     sw = torch.empty((E, N), dtype=torch.float32, device="cuda")
     pk.pk_moe_quant_weights(W_dev, wq, sw)
     torch.cuda.synchronize()
@@ -75,7 +87,7 @@ def test_quant_weights_bit_exact(gpu_lib, E, D, N):
     wq, sw = _gpu_quant_weights(gpu_lib, u16_to_bf16_dev(W))
     q_ref, s_ref = oracle.quant_cols(W)
     assert np.array_equal(sw.cpu().numpy().view(np.uint32), s_ref.view(np.uint32))
-    assert np.array_equal(wq.cpu().numpy(), q_ref)
+    assert np.array_equal(wq.cpu().numpy(), to_blocked(q_ref))
 
 
 def _fp8_case(pk, x, topk, W, E, rows=None):
@@ -91,12 +103,14 @@ def _fp8_case(pk, x, topk, W, E, rows=None):
     ref = oracle.run(topk, E)
     xq, sx = oracle.quant_rows(x)
     wq, sw = oracle.quant_cols(W)
-    assert np.array_equal(xq_g.cpu().numpy(), xq) and np.array_equal(wq_g.cpu().numpy(), wq)
+    assert np.array_equal(xq_g.cpu().numpy(), xq)
+    assert np.array_equal(wq_g.cpu().numpy(), to_blocked(wq))
     assert np.array_equal(sx_g.cpu().numpy(), sx) and np.array_equal(sw_g.cpu().numpy(), sw)
     del xq_g, wq_g
     out = torch.full((T * k, De), float("nan"), dtype=torch.bfloat16, device="cuda")
     pk.pk_moe_dispatch_gemm_fp8(_u8_dev(xq), torch.from_numpy(sx).cuda(), md.perm, md.offsets,
-                                _u8_dev(wq), torch.from_numpy(sw).cuda(), k, out, md.status)
+                                _u8_dev(to_blocked(wq)), torch.from_numpy(sw).cuda(), k, out,
+                                md.status)
     torch.cuda.synchronize()
     assert md.status_code() == 0, pk.pk_status_str(md.status_code())
     assert np.array_equal(md.perm[:T * k].cpu().numpy().astype(np.int64), ref["perm"])
@@ -144,7 +158,8 @@ def test_fp8_gemm_bad_perm_entry_sets_status(gpu_lib):
     perm[3] = T * k + 5
     out = torch.zeros((T * k, De), dtype=torch.bfloat16, device="cuda")
     pk.pk_moe_dispatch_gemm_fp8(_u8_dev(xq), torch.from_numpy(sx).cuda(), perm, md.offsets,
-                                _u8_dev(wq), torch.from_numpy(sw).cuda(), k, out, md.status)
+                                _u8_dev(to_blocked(wq)), torch.from_numpy(sw).cuda(), k, out,
+                                md.status)
     torch.cuda.synchronize()
     assert md.status_code() == pk.PK_ERR_BAD_INDEX
     assert bool(torch.isfinite(out.float()).all())
@@ -171,7 +186,7 @@ def test_fp8_full_size_ep_sampled(gpu_lib):
     wq_g, sw_g = _gpu_quant_weights(pk, Wd)
     del Wd
     q_ref, s_ref = oracle.quant_cols(W[experts])
-    assert np.array_equal(wq_g[experts].cpu().numpy(), q_ref)
+    assert np.array_equal(wq_g[experts].cpu().numpy(), to_blocked(q_ref))
     assert np.array_equal(sw_g[experts].cpu().numpy(), s_ref)
     out = torch.empty((wl.T * wl.k, wl.De), dtype=torch.bfloat16, device="cuda")
     pk.pk_moe_dispatch_gemm_fp8(xq_g, sx_g, md.perm, md.offsets, wq_g, sw_g, wl.k, out,
