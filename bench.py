@@ -35,6 +35,11 @@ import numpy as np  # noqa: E402
 METRIC = "dispatch+expert-GEMM TFLOP/s and % of GB300 BF16 peak at T=8192 D=7168 E=256 k=8"
 UNIT = "TFLOP/s"
 PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# source file and ncu summary prefix of each dispatch GEMM kernel
+GEMM_KERNELS = {
+    "single": ("dispatch_gemm.cu", "dispatch_gemm", "k_dispatch_gemm"),
+    "pair": ("dispatch_gemm_pair.cu", "dispatch_gemm_pair", "k_dispatch_gemm_pair"),
+}
 GEMM_SOURCE = os.path.join(ROOT, "moe_token_dispatch_gb300", "csrc", "dispatch_gemm.cu")
 
 
@@ -61,18 +66,20 @@ def source_digest(path=GEMM_SOURCE) -> str:
 TRAFFIC_SCALED_FROM = {"ep": ("ep32", 256 / 32), "decode": ("decode32", 252 / 32)}
 
 
-def profiled_traffic(workload: str):
+def profiled_traffic(workload: str, kernel: str = "single"):
     """DRAM bytes per GEMM launch from the committed ncu summary, if it was
     taken on the current kernel source; else None."""
+    src, prefix, _ = GEMM_KERNELS[kernel]
     name, scale = TRAFFIC_SCALED_FROM.get(workload, (workload, 1.0))
-    path = os.path.join(ROOT, "profiles", f"dispatch_gemm_{name}.md")
+    path = os.path.join(ROOT, "profiles", f"{prefix}_{name}.md")
     try:
         text = open(path).read()
     except OSError:
         return None
     m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
     s = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", text)
-    if not m or not s or s.group(1) != source_digest():
+    src_path = os.path.join(ROOT, "moe_token_dispatch_gb300", "csrc", src)
+    if not m or not s or s.group(1) != source_digest(src_path):
         return None
     return float(m.group(1)) * scale
 
@@ -259,6 +266,8 @@ def run_ours(args, wl):
     import torch
     import inputgen as ig
     import moe_token_dispatch_gb300 as pk
+    pk.pk_moe_set_gemm_kernel({"auto": pk.PK_GEMM_KERNEL_AUTO, "single": pk.PK_GEMM_KERNEL_SINGLE,
+                               "pair": pk.PK_GEMM_KERNEL_PAIR}[args.gemm_kernel])
 
     rank, world, local = dist_env()
     torch.cuda.set_device(local)
@@ -373,24 +382,25 @@ def run_ours(args, wl):
     achieved_gbs = alg_bytes / (gemm_avg_ms * 1e-3) / 1e9
     gemm_tflops = flops / (gemm_avg_ms * 1e-3) / 1e12
     value = world * flops / (step_ms * 1e-3) / 1e12
-    traffic = profiled_traffic(wl.name)
+    kernel = "single" if args.gemm_kernel == "single" else "pair"
+    traffic = profiled_traffic(wl.name, kernel)
 
     cpu_value, cpu_info = oracle_sample(case, wl, args.cpu_seconds, os.cpu_count() or 1)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
         "warmup": max(3, args.warmup), "ms_per_step": step_ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": config_of(wl),
+        "config": dict(config_of(wl), gemm_kernel=kernel),
         "pct_bf16_peak": 100.0 * value / world / peaks["bf16_tflops"],
         "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": peaks["hbm_gbs"],
                      "unit": "GB/s", "frac": achieved_gbs / peaks["hbm_gbs"],
                      "traffic": traffic, "peak_kind": peak_kind,
-                     "kernel": "k_dispatch_gemm", "kernel_ms": gemm_avg_ms,
+                     "kernel": GEMM_KERNELS[kernel][2], "kernel_ms": gemm_avg_ms,
                      "algorithmic_bytes": alg_bytes, "bytes_breakdown": b,
                      "tensor": {"achieved": gemm_tflops, "peak": peaks["bf16_tflops"],
                                 "peak_sustained": peaks.get("bf16_tflops_sustained"),
                                 "unit": "TFLOP/s", "frac": gemm_tflops / peaks["bf16_tflops"]}},
-        "kernel_share": {"k_dispatch_gemm": gemm_avg_ms / step_ms},
+        "kernel_share": {GEMM_KERNELS[kernel][2]: gemm_avg_ms / step_ms},
         "cpu_baseline": {"value": cpu_value, "unit": UNIT, "cores": os.cpu_count() or 1,
                          "kind": "oracle",
                          "sample": f"full routing + float64 GEMM of {cpu_info['rows']} random "
@@ -413,6 +423,8 @@ def run_op(args, wl):
     import torch
     import inputgen as ig
     import moe_token_dispatch_gb300 as pk
+    pk.pk_moe_set_gemm_kernel({"auto": pk.PK_GEMM_KERNEL_AUTO, "single": pk.PK_GEMM_KERNEL_SINGLE,
+                               "pair": pk.PK_GEMM_KERNEL_PAIR}[args.gemm_kernel])
 
     torch.cuda.set_device(0)
     dev = torch.device("cuda", 0)
@@ -528,6 +540,9 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="ep")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--gemm-kernel", choices=["auto", "single", "pair"], default="auto",
+                    help="dispatch GEMM kernel: auto (the CTA-pair kernel), single (one CTA per "
+                         "SM) or pair")
     ap.add_argument("--op", default="dispatch_gemm",
                     choices=["dispatch_gemm", "router", "combine", "grouped_gemm", "fp8_gemm"],
                     help="dispatch_gemm: the benchmark step; the others time one kernel")

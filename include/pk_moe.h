@@ -265,6 +265,21 @@ int pk_moe_route_noalloc(const int32_t* topk_idx, int32_t T, int32_t k, int32_t 
                          int32_t* inv_perm, int32_t* status_word, void* stream);
 
 /*
+ * Kernel used by pk_moe_dispatch_gemm and pk_moe_dispatch_gemm_fp8 for
+ * later calls from this process (both compute the same result, within
+ * fp32 summation order):
+ *   PK_GEMM_KERNEL_AUTO    default: the CTA-pair kernel
+ *   PK_GEMM_KERNEL_SINGLE  one CTA per SM, tcgen05.mma.cta_group::1 (M = 128)
+ *   PK_GEMM_KERNEL_PAIR    2-CTA clusters, tcgen05.mma.cta_group::2 (M = 256):
+ *                          each SM loads its own rows and half of each W tile
+ * Returns PK_ERR_INVALID_ARG for any other value.
+ */
+#define PK_GEMM_KERNEL_AUTO 0
+#define PK_GEMM_KERNEL_SINGLE 1
+#define PK_GEMM_KERNEL_PAIR 2
+int pk_moe_set_gemm_kernel(int kernel);
+
+/*
  * Limit, in nanoseconds, on every pipeline wait inside the GEMM kernel
  * (default 4e9). A wait that runs out sets PK_ERR_TIMEOUT and the kernel
  * drains its own copies and returns. Applies to later launches from this

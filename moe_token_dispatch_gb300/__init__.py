@@ -14,6 +14,9 @@ from ._binding import (  # noqa: F401
     PK_ERR_INVALID_ARG,
     PK_ERR_TIMEOUT,
     PK_ERR_UNSUPPORTED,
+    PK_GEMM_KERNEL_AUTO,
+    PK_GEMM_KERNEL_PAIR,
+    PK_GEMM_KERNEL_SINGLE,
     PK_MAX_EXPERTS,
     PK_NOALLOC_SCRATCH_BYTES,
     PK_OK,
@@ -33,6 +36,7 @@ from ._binding import (  # noqa: F401
     pk_moe_route_counts,
     pk_moe_route_noalloc,
     pk_moe_router_topk,
+    pk_moe_set_gemm_kernel,
     pk_moe_set_wait_limit_ns,
     pk_moe_workspace_bytes,
     pk_status_str,

@@ -23,6 +23,9 @@ PK_ERR_BAD_INDEX = 5
 PK_MAX_EXPERTS = 4096
 PK_NOALLOC_SCRATCH_BYTES = 1 << 20
 PK_ROUTER_MAX_EXPERTS = 1024
+PK_GEMM_KERNEL_AUTO = 0
+PK_GEMM_KERNEL_SINGLE = 1
+PK_GEMM_KERNEL_PAIR = 2
 
 
 class PkError(RuntimeError):
@@ -65,6 +68,8 @@ def _load():
     lib.pk_moe_router_topk.argtypes = [P, I32, I32, I32, P, P, P]
     lib.pk_moe_combine.restype = ctypes.c_int
     lib.pk_moe_combine.argtypes = [P, P, P, I32, I32, I32, P, P, P]
+    lib.pk_moe_set_gemm_kernel.restype = ctypes.c_int
+    lib.pk_moe_set_gemm_kernel.argtypes = [ctypes.c_int]
     lib.pk_moe_set_wait_limit_ns.restype = None
     lib.pk_moe_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
     lib.pk_debug_bounded_wait.restype = ctypes.c_int
@@ -266,6 +271,10 @@ def pk_moe_route_noalloc(topk_idx: torch.Tensor, E: int, expert_offsets: torch.T
         _ptr(inv_perm, torch.int32, "inv_perm", T * k),
         _ptr(status_word, torch.int32, "status_word", 1), _stream(stream))
     _check(rc, "pk_moe_route_noalloc")
+
+
+def pk_moe_set_gemm_kernel(kernel: int) -> None:
+    _check(lib.pk_moe_set_gemm_kernel(int(kernel)), "pk_moe_set_gemm_kernel")
 
 
 def pk_moe_set_wait_limit_ns(limit_ns: int) -> None:

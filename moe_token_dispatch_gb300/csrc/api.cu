@@ -12,6 +12,12 @@ namespace {
 
 constexpr uint64_t kDefaultWaitLimitNs = 4000000000ull;
 std::atomic<uint64_t> g_wait_limit_ns{kDefaultWaitLimitNs};
+std::atomic<int> g_gemm_kernel{PK_GEMM_KERNEL_AUTO};
+
+bool use_pair() {
+    const int v = g_gemm_kernel.load(std::memory_order_relaxed);
+    return v != PK_GEMM_KERNEL_SINGLE;
+}
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -84,9 +90,13 @@ int pk_moe_dispatch_gemm(const uint16_t* x, const int32_t* perm, const int32_t* 
     if (R == 0) return PK_OK;
     if (!x || !perm || !expert_offsets || !W || !out) return PK_ERR_INVALID_ARG;
     if (!aligned16(x) || !aligned16(W) || !aligned16(out)) return PK_ERR_INVALID_ARG;
-    return pk::launch_dispatch_gemm(x, perm, expert_offsets, W, T, k, D, E, D_expert, out,
-                                    status_word, static_cast<cudaStream_t>(stream),
-                                    g_wait_limit_ns.load(std::memory_order_relaxed));
+    const uint64_t limit = g_wait_limit_ns.load(std::memory_order_relaxed);
+    if (use_pair())
+        return pk::launch_dispatch_gemm_pair(false, x, nullptr, perm, expert_offsets, W, nullptr, T,
+                                             k, D, E, D_expert, out, status_word,
+                                             static_cast<cudaStream_t>(stream), limit);
+    return pk::launch_dispatch_gemm_single(x, perm, expert_offsets, W, T, k, D, E, D_expert, out,
+                                           status_word, static_cast<cudaStream_t>(stream), limit);
 }
 
 int pk_moe_dispatch_gemm_fp8(const uint8_t* xq, const float* sx, const int32_t* perm,
@@ -102,10 +112,14 @@ int pk_moe_dispatch_gemm_fp8(const uint8_t* xq, const float* sx, const int32_t* 
     if (!aligned16(xq) || !aligned16(wq) || !aligned16(sw) || !aligned16(out))
         return PK_ERR_INVALID_ARG;
     if (pk_moe_fp8_weight_bytes(E, D, D_expert) >= (size_t{1} << 38)) return PK_ERR_UNSUPPORTED;
-    return pk::launch_dispatch_gemm_fp8(xq, sx, perm, expert_offsets, wq, sw, T, k, D, E,
-                                        D_expert, out, status_word,
-                                        static_cast<cudaStream_t>(stream),
-                                        g_wait_limit_ns.load(std::memory_order_relaxed));
+    const uint64_t limit = g_wait_limit_ns.load(std::memory_order_relaxed);
+    if (use_pair())
+        return pk::launch_dispatch_gemm_pair(true, xq, sx, perm, expert_offsets, wq, sw, T, k, D, E,
+                                             D_expert, out, status_word,
+                                             static_cast<cudaStream_t>(stream), limit);
+    return pk::launch_dispatch_gemm_fp8_single(xq, sx, perm, expert_offsets, wq, sw, T, k, D, E,
+                                               D_expert, out, status_word,
+                                               static_cast<cudaStream_t>(stream), limit);
 }
 
 int pk_moe_quant_rows(const uint16_t* x, int32_t T, int32_t D, uint8_t* xq, float* sx,
@@ -169,6 +183,14 @@ int pk_moe_combine(const uint16_t* src, const int32_t* inv_perm, const float* ga
     cudaError_t err = pk::launch_combine(src, inv_perm, gates, T, k, C, y, status_word,
                                          static_cast<cudaStream_t>(stream));
     return err == cudaSuccess ? PK_OK : PK_ERR_CUDA;
+}
+
+int pk_moe_set_gemm_kernel(int kernel) {
+    if (kernel != PK_GEMM_KERNEL_AUTO && kernel != PK_GEMM_KERNEL_SINGLE &&
+        kernel != PK_GEMM_KERNEL_PAIR)
+        return PK_ERR_INVALID_ARG;
+    g_gemm_kernel.store(kernel, std::memory_order_relaxed);
+    return PK_OK;
 }
 
 void pk_moe_set_wait_limit_ns(uint64_t limit_ns) {

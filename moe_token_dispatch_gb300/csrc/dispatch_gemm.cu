@@ -598,6 +598,40 @@ PFN_cuTensorMapEncodeTiled_v12000 encoder() {
 
 }  // namespace
 
+// Tensor map of the expert weights. bf16 W [E, D, De]: a 3-D map {De, D, E}
+// with 64 x 64 boxes. FP8 codes in the blocked layout: a [rows, 128] byte
+// matrix of 64-row boxes (rows = E * ceil(De/64) * ceil(D/128) * 64). Both
+// with 128-byte swizzle; out-of-range boxes read zeros.
+int make_w_map(bool fp8, const void* W, int32_t D, int32_t E, int32_t De, CUtensorMap* wmap) {
+    using namespace dg;
+    auto enc = encoder();
+    if (!enc) return PK_ERR_CUDA;
+    if (fp8) {
+        const uint64_t rows = static_cast<uint64_t>(E) * ((De + B_BOX - 1) / B_BOX) *
+                              ((D + ROW_BYTES - 1) / ROW_BYTES) * B_BOX;
+        cuuint64_t dims[2] = {static_cast<cuuint64_t>(ROW_BYTES), static_cast<cuuint64_t>(rows)};
+        cuuint64_t strides[1] = {static_cast<cuuint64_t>(ROW_BYTES)};
+        cuuint32_t box[2] = {ROW_BYTES, B_BOX};
+        cuuint32_t es[2] = {1, 1};
+        if (enc(wmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(W), dims, strides, box,
+                es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return PK_ERR_UNSUPPORTED;
+    } else {
+        cuuint64_t dims[3] = {static_cast<cuuint64_t>(De), static_cast<cuuint64_t>(D),
+                              static_cast<cuuint64_t>(E)};
+        cuuint64_t strides[2] = {static_cast<cuuint64_t>(De) * 2,
+                                 static_cast<cuuint64_t>(D) * static_cast<cuuint64_t>(De) * 2};
+        cuuint32_t box[3] = {B_BOX, BK, 1};
+        cuuint32_t es[3] = {1, 1, 1};
+        if (enc(wmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(W), dims, strides,
+                box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return PK_ERR_UNSUPPORTED;
+    }
+    return PK_OK;
+}
+
 namespace {
 
 // Builds the tensor maps and launches one instantiation. A is x (gathered
@@ -636,30 +670,8 @@ int launch_common(bool gather, bool fp8, const void* A, const float* sx, const i
     }
 
     CUtensorMap wmap, amap;
-    if (fp8) {
-        // blocked W codes: a [rows, 128] matrix of 64-row boxes, 128-byte swizzle
-        const uint64_t rows = static_cast<uint64_t>(E) * ((De + B_BOX - 1) / B_BOX) *
-                              ((D + ROW_BYTES - 1) / ROW_BYTES) * B_BOX;
-        cuuint64_t dims[2] = {static_cast<cuuint64_t>(ROW_BYTES), static_cast<cuuint64_t>(rows)};
-        cuuint64_t strides[1] = {static_cast<cuuint64_t>(ROW_BYTES)};
-        cuuint32_t box[2] = {ROW_BYTES, B_BOX};
-        cuuint32_t es[2] = {1, 1};
-        if (enc(&wmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(W), dims, strides, box,
-                es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-            return PK_ERR_UNSUPPORTED;
-    } else {
-        cuuint64_t dims[3] = {static_cast<cuuint64_t>(De), static_cast<cuuint64_t>(D),
-                              static_cast<cuuint64_t>(E)};
-        cuuint64_t strides[2] = {static_cast<cuuint64_t>(De) * 2,
-                                 static_cast<cuuint64_t>(D) * static_cast<cuuint64_t>(De) * 2};
-        cuuint32_t box[3] = {B_BOX, BK, 1};
-        cuuint32_t es[3] = {1, 1, 1};
-        if (enc(&wmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(W), dims, strides,
-                box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-            return PK_ERR_UNSUPPORTED;
-    }
+    const int rc = make_w_map(fp8, W, D, E, De, &wmap);
+    if (rc != PK_OK) return rc;
     if (gather) {
         amap = wmap;  // unused
     } else {
@@ -690,19 +702,19 @@ int launch_common(bool gather, bool fp8, const void* A, const float* sx, const i
 
 }  // namespace
 
-int launch_dispatch_gemm(const uint16_t* x, const int32_t* perm, const int32_t* offsets,
-                         const uint16_t* W, int32_t T, int32_t k, int32_t D, int32_t E,
-                         int32_t De, uint16_t* out, int32_t* status, cudaStream_t stream,
-                         uint64_t wait_limit_ns) {
+int launch_dispatch_gemm_single(const uint16_t* x, const int32_t* perm, const int32_t* offsets,
+                                const uint16_t* W, int32_t T, int32_t k, int32_t D, int32_t E,
+                                int32_t De, uint16_t* out, int32_t* status, cudaStream_t stream,
+                                uint64_t wait_limit_ns) {
     return launch_common(true, false, x, nullptr, perm, offsets, W, nullptr, T, k, D, E, De, out,
                          status, stream, wait_limit_ns);
 }
 
-int launch_dispatch_gemm_fp8(const uint8_t* xq, const float* sx, const int32_t* perm,
-                             const int32_t* offsets, const uint8_t* wq, const float* sw,
-                             int32_t T, int32_t k, int32_t D, int32_t E, int32_t De,
-                             uint16_t* out, int32_t* status, cudaStream_t stream,
-                             uint64_t wait_limit_ns) {
+int launch_dispatch_gemm_fp8_single(const uint8_t* xq, const float* sx, const int32_t* perm,
+                                    const int32_t* offsets, const uint8_t* wq, const float* sw,
+                                    int32_t T, int32_t k, int32_t D, int32_t E, int32_t De,
+                                    uint16_t* out, int32_t* status, cudaStream_t stream,
+                                    uint64_t wait_limit_ns) {
     return launch_common(true, true, xq, sx, perm, offsets, wq, sw, T, k, D, E, De, out, status,
                          stream, wait_limit_ns);
 }

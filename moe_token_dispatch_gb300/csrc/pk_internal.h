@@ -1,6 +1,7 @@
 // Host-side declarations shared by the translation units of libpkmoe.so.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -22,19 +23,29 @@ cudaError_t launch_build_perm(const int32_t* topk, int32_t R, int32_t E,
                               const int32_t* blockbase, int32_t* perm, int32_t* inv_perm,
                               int32_t* status, cudaStream_t stream);
 
-// Dispatch GEMM. Returns PK_OK or a pk_status for host-side failures.
-int launch_dispatch_gemm(const uint16_t* x, const int32_t* perm, const int32_t* offsets,
+// Dispatch GEMM, one-CTA kernel. Returns PK_OK or a pk_status for host-side
+// failures.
+int launch_dispatch_gemm_single(const uint16_t* x, const int32_t* perm, const int32_t* offsets,
                          const uint16_t* W, int32_t T, int32_t k, int32_t D, int32_t E,
                          int32_t De, uint16_t* out, int32_t* status, cudaStream_t stream,
                          uint64_t wait_limit_ns);
 
 // FP8 dispatch GEMM: E4M3 codes xq [T, D] and wq [E, De, D] with fp32 scales
 // sx [T] and sw [E, De].
-int launch_dispatch_gemm_fp8(const uint8_t* xq, const float* sx, const int32_t* perm,
+int launch_dispatch_gemm_fp8_single(const uint8_t* xq, const float* sx, const int32_t* perm,
                              const int32_t* offsets, const uint8_t* wq, const float* sw,
                              int32_t T, int32_t k, int32_t D, int32_t E, int32_t De,
                              uint16_t* out, int32_t* status, cudaStream_t stream,
                              uint64_t wait_limit_ns);
+
+// Dispatch GEMM on CTA pairs (bf16, or FP8 codes with scales sx, sw).
+int launch_dispatch_gemm_pair(bool fp8, const void* x, const float* sx, const int32_t* perm,
+                              const int32_t* offsets, const void* W, const float* sw, int32_t T,
+                              int32_t k, int32_t D, int32_t E, int32_t De, uint16_t* out,
+                              int32_t* status, cudaStream_t stream, uint64_t wait_limit_ns);
+
+// Tensor map of bf16 W [E, D, De] or of the blocked FP8 codes.
+int make_w_map(bool fp8, const void* W, int32_t D, int32_t E, int32_t De, CUtensorMap* wmap);
 
 // E4M3 quantisation with one scale per row of x / per (expert, column) of W.
 cudaError_t launch_quant_rows(const uint16_t* x, int32_t T, int32_t D, uint8_t* q, float* scale,

@@ -23,3 +23,14 @@ def gpu_lib():
     __graft_entry__._build_module().build()
     import moe_token_dispatch_gb300 as pk
     return pk
+
+
+@pytest.fixture(params=["pair", "single"])
+def gemm_kernel(request, gpu_lib):
+    """Runs a GEMM test once with the CTA-pair kernel and once with the
+    one-CTA kernel (both behind the same C entry points)."""
+    pk = gpu_lib
+    pk.pk_moe_set_gemm_kernel(pk.PK_GEMM_KERNEL_PAIR if request.param == "pair"
+                              else pk.PK_GEMM_KERNEL_SINGLE)
+    yield request.param
+    pk.pk_moe_set_gemm_kernel(pk.PK_GEMM_KERNEL_AUTO)

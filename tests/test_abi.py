@@ -136,3 +136,11 @@ def test_fp8_weight_bytes(lib):
     assert L.pk_moe_fp8_weight_bytes(256, 7168, 2048) == 256 * 32 * 56 * 8192
     assert L.pk_moe_fp8_weight_bytes(3, 200, 136) == 3 * 3 * 2 * 8192
     assert L.pk_moe_fp8_weight_bytes(0, 16, 8) == 0
+
+
+def test_set_gemm_kernel(lib):
+    L = _raw(lib)
+    assert L.pk_moe_set_gemm_kernel(7) == 1
+    assert L.pk_moe_set_gemm_kernel(-1) == 1
+    for v in (1, 2, 0):
+        assert L.pk_moe_set_gemm_kernel(v) == 0

@@ -130,23 +130,24 @@ FP8_MULTI_TILE = [
     (1000, 64, 2, 2, 256),      # 1000 rows per expert: groups of two m-tiles
     (96, 16, 5, 2, 8),          # smallest legal D and De
     (2048, 1280, 32, 4, 384),   # many experts, ring wraps many times
+    (770, 320, 2, 1, 600),      # half-empty CTA pair; De = 512 + 88
 ]
 
 
 @pytest.mark.parametrize("T,D,E,k,De", FP8_MULTI_TILE)
-def test_fp8_gemm_all_rows(gpu_lib, T, D, E, k, De):
+def test_fp8_gemm_all_rows(gpu_lib, gemm_kernel, T, D, E, k, De):
     c = ig.make_case(ig.custom(T=T, D=D, E=E, k=k, De=De, seed=5))
     _fp8_case(gpu_lib, c.x, c.topk, c.W, E)
 
 
-def test_fp8_gemm_skew_and_empty_experts(gpu_lib):
+def test_fp8_gemm_skew_and_empty_experts(gpu_lib, gemm_kernel):
     c = ig.make_case(ig.custom(T=1500, D=256, E=16, k=2, De=320, zipf_s=1.4, seed=9))
     counts = np.bincount(c.topk.ravel(), minlength=16)
     assert counts.max() > 384  # at least one expert with groups of m-tiles
     _fp8_case(gpu_lib, c.x, c.topk, c.W, 16)
 
 
-def test_fp8_gemm_bad_perm_entry_sets_status(gpu_lib):
+def test_fp8_gemm_bad_perm_entry_sets_status(gpu_lib, gemm_kernel):
     pk = gpu_lib
     T, k, E, D, De = 64, 2, 4, 64, 64
     c = ig.make_case(ig.custom(T=T, D=D, E=E, k=k, De=De, seed=2))

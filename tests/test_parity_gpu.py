@@ -22,7 +22,7 @@ def _case(T, D, E, k, De, zipf=0.0, seed=0):
     return c.x, c.topk, c.W
 
 
-def test_tiny_workload_all_rows(gpu_lib):
+def test_tiny_workload_all_rows(gpu_lib, gemm_kernel):
     wl = ig.WORKLOADS["tiny"]
     c = ig.make_case(wl)
     check_case(gpu_lib, c.x, c.topk, c.W, wl.E)
@@ -39,21 +39,22 @@ MULTI_TILE = [
     (300, 1024, 8, 3, 1408),    # mid-like widths, 16 K-steps
     (1000, 64, 2, 2, 256),      # 1000 rows per expert: 8 m-tiles, 4 groups
     (96, 8, 5, 2, 8),           # smallest legal D and De
+    (770, 320, 2, 1, 600),      # 3 and 4 m-tiles: a half-empty CTA pair; De = 512 + 88
 ]
 
 
 @pytest.mark.parametrize("T,D,E,k,De", MULTI_TILE)
-def test_multi_tile_all_rows(gpu_lib, T, D, E, k, De):
+def test_multi_tile_all_rows(gpu_lib, gemm_kernel, T, D, E, k, De):
     x, topk, W = _case(T, D, E, k, De)
     check_case(gpu_lib, x, topk, W, E)
 
 
-def test_single_token_single_expert(gpu_lib):
+def test_single_token_single_expert(gpu_lib, gemm_kernel):
     x, topk, W = _case(1, 64, 1, 1, 64)
     check_case(gpu_lib, x, topk, W, 1)
 
 
-def test_empty_experts_and_one_expert_takes_all(gpu_lib):
+def test_empty_experts_and_one_expert_takes_all(gpu_lib, gemm_kernel):
     T, D, E, k, De = 333, 128, 16, 1, 192
     x, _, W = _case(T, D, E, k, De)
     topk = np.full((T, k), 7, dtype=np.int32)
@@ -61,7 +62,7 @@ def test_empty_experts_and_one_expert_takes_all(gpu_lib):
     assert res["counts"].tolist() == [0] * 7 + [T] + [0] * 8
 
 
-def test_duplicate_experts_in_one_token(gpu_lib):
+def test_duplicate_experts_in_one_token(gpu_lib, gemm_kernel):
     T, D, E, k, De = 77, 64, 4, 3, 64
     x, _, W = _case(T, D, E, k, De)
     rng = np.random.default_rng(11)
@@ -70,7 +71,7 @@ def test_duplicate_experts_in_one_token(gpu_lib):
     check_case(gpu_lib, x, topk, W, E)
 
 
-def test_skewed_routing_small(gpu_lib):
+def test_skewed_routing_small(gpu_lib, gemm_kernel):
     x, topk, W = _case(2048, 256, 32, 4, 384, zipf=1.2)
     counts = np.bincount(topk.ravel(), minlength=32)
     assert counts.max() > 4 * counts.mean()
@@ -91,7 +92,7 @@ def test_zero_tokens(gpu_lib):
     assert md.offsets.tolist() == [0] * 9 and md.counts.tolist() == [0] * 8
 
 
-def test_bad_index_sets_status(gpu_lib):
+def test_bad_index_sets_status(gpu_lib, gemm_kernel):
     pk = gpu_lib
     T, k, E = 40, 2, 4
     topk = np.random.default_rng(1).integers(0, E, size=(T, k)).astype(np.int32)
@@ -106,7 +107,7 @@ def test_bad_index_sets_status(gpu_lib):
     assert md.counts.cpu().numpy().tolist() == np.bincount(valid, minlength=E).tolist()
 
 
-def test_repeat_runs_are_bitwise_identical(gpu_lib):
+def test_repeat_runs_are_bitwise_identical(gpu_lib, gemm_kernel):
     x, topk, W = _case(512, 576, 4, 2, 640)
     Wd = u16_to_bf16_dev(W)
     a = run_gpu(gpu_lib, x, topk, Wd, 4, 640)
@@ -132,7 +133,7 @@ def test_bounded_wait_times_out_and_context_survives(gpu_lib):
 
 
 # ------------------------------------------------- the five named workloads
-def test_mid_workload(gpu_lib):
+def test_mid_workload(gpu_lib, gemm_kernel):
     wl = ig.WORKLOADS["mid"]
     c = ig.make_case(wl)
     rows = boundary_rows(oracle.route_counts(c.topk, wl.E)[1], np.random.default_rng(0), 256)
