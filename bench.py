@@ -382,7 +382,7 @@ def run_ours(args, wl):
     achieved_gbs = alg_bytes / (gemm_avg_ms * 1e-3) / 1e9
     gemm_tflops = flops / (gemm_avg_ms * 1e-3) / 1e12
     value = world * flops / (step_ms * 1e-3) / 1e12
-    kernel = "single" if args.gemm_kernel == "single" else "pair"
+    kernel = "pair" if args.gemm_kernel == "pair" else "single"
     traffic = profiled_traffic(wl.name, kernel)
 
     cpu_value, cpu_info = oracle_sample(case, wl, args.cpu_seconds, os.cpu_count() or 1)
@@ -541,8 +541,8 @@ def main(argv=None):
     ap.add_argument("--workload", default="ep")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--gemm-kernel", choices=["auto", "single", "pair"], default="auto",
-                    help="dispatch GEMM kernel: auto (the CTA-pair kernel), single (one CTA per "
-                         "SM) or pair")
+                    help="dispatch GEMM kernel: auto (= single), single (one CTA per SM) or pair "
+                         "(2-CTA clusters)")
     ap.add_argument("--op", default="dispatch_gemm",
                     choices=["dispatch_gemm", "router", "combine", "grouped_gemm", "fp8_gemm"],
                     help="dispatch_gemm: the benchmark step; the others time one kernel")

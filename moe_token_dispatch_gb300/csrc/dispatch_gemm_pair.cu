@@ -26,6 +26,12 @@
 // Four 48 KiB stages. An expert's last m-tile pair may be half empty (odd
 // number of m-tiles): the idle CTA still supplies its B halves; its rows are
 // neither gathered nor stored.
+//
+// Measured on GB300 against the one-CTA kernel it is slower on every
+// workload (ep 2.21 vs 1.79 ms, decode 1.36 vs 1.1 ms, FP8 ep 1.16 vs 1.00
+// ms): both run at the latency of their ring, and every K-step here adds a
+// cross-SM hop (relay to rank 0, multicast commit back) and waits for the
+// slower of two SMs. It stays as an option behind pk_moe_set_gemm_kernel.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
