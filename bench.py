@@ -66,12 +66,19 @@ def source_digest(path=GEMM_SOURCE) -> str:
 TRAFFIC_SCALED_FROM = {"ep": ("ep32", 256 / 32), "decode": ("decode32", 252 / 32)}
 
 
-def profiled_traffic(workload: str, kernel: str = "single"):
-    """DRAM bytes per GEMM launch from the committed ncu summary, if it was
-    taken on the current kernel source; else None."""
-    src, prefix, _ = GEMM_KERNELS[kernel]
-    name, scale = TRAFFIC_SCALED_FROM.get(workload, (workload, 1.0))
+def profiled_traffic(workload: str, kernel: str = "single", prefix: str | None = None,
+                     src: str | None = None):
+    """DRAM bytes per launch from the committed ncu summary
+    profiles/<prefix>_<workload>.md, if it was taken on the current kernel
+    source; else None. Defaults: the dispatch GEMM kernel `kernel`."""
+    if prefix is None:
+        src, prefix, _ = GEMM_KERNELS[kernel]
+    # a capture of the workload itself, else of its smaller stand-in, scaled
+    name, scale = workload, 1.0
     path = os.path.join(ROOT, "profiles", f"{prefix}_{name}.md")
+    if not os.path.exists(path) and workload in TRAFFIC_SCALED_FROM:
+        name, scale = TRAFFIC_SCALED_FROM[workload]
+        path = os.path.join(ROOT, "profiles", f"{prefix}_{name}.md")
     try:
         text = open(path).read()
     except OSError:
@@ -506,11 +513,17 @@ def run_op(args, wl):
     ms = sorted(a.elapsed_time(b) for a, b in ev)
     med = ms[len(ms) // 2]
     gbs = alg_bytes / (med * 1e-3) / 1e9
+    # ncu summaries of the kernels beside the step (prefix, source file)
+    op_profile = {"combine": ("combine", "combine_router.cu"),
+                  "grouped_gemm": ("grouped_gemm", "dispatch_gemm.cu"),
+                  "fp8_gemm": ("fp8_dispatch_gemm", "dispatch_gemm.cu")}.get(args.op)
+    traffic = (profiled_traffic(wl.name, prefix=op_profile[0], src=op_profile[1])
+               if op_profile else None)
     line = {"op": args.op, "metric": metric, "workload": wl.name, "ms_median": med,
             "ms_p10": ms[len(ms) // 10], "ms_p90": ms[(9 * len(ms)) // 10], "steps": args.steps,
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                          "frac": gbs / peaks["hbm_gbs"], "algorithmic_bytes": alg_bytes,
-                         "peak_kind": peak_kind}}
+                         "traffic": traffic, "peak_kind": peak_kind}}
     if flops:
         tf = flops / (med * 1e-3) / 1e12
         line["value"], line["unit"] = tf, "TFLOP/s"
