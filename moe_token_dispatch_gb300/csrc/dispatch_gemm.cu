@@ -11,23 +11,24 @@
 //              columns.
 //   warp 4     MMA issuer (one thread) and TMEM owner: tcgen05.mma M=128 x
 //              N=bn x K=16 per m-tile into fp32 accumulators in TMEM; each
-//              commit frees a shared-memory stage or hands the unit's
+//              commit frees a shared-memory slot or hands the unit's
 //              accumulators to the epilogue.
 //   warp 5     W producer (one thread): per K-step of 64 rows, TMA-loads the
 //              W_e tile [64 x bn] as 64x64 boxes, 128-byte swizzle (MN-major
-//              operand), and asks TMA to prefetch into L2 the W boxes of the
-//              K-step W_PREFETCH steps ahead, so HBM latency is covered by L2
-//              rather than by shared-memory stages.
+//              operand).
 //   warps 6,7,9,10  dispatch: gather the unit's routed x rows with 16-byte
 //              cp.async into K-major 128-byte-swizzled tiles (each warp
 //              instruction moves four whole 128-byte row segments); each
-//              thread's copies arrive on the stage's barrier when they land,
+//              thread's copies arrive on the slots' barriers when they land,
 //              and the MMA thread fences them into the async proxy after its
 //              wait, before the tensor cores read them.
 // Warp 8 only waits at the final barrier: warps share an SM sub-partition
 // with the warps whose index is equal mod 4, and this keeps the busy gather
 // warps off the MMA issuer's sub-partition.
-// Three 64 KiB stages (full/empty mbarriers) connect producers and MMA.
+// Two rings of shared-memory slots (full/empty mbarriers) connect producers
+// and MMA: four 32 KiB W slots and three 32 KiB A slots, one of each per
+// K-step. W comes from HBM and takes longest to arrive, so it runs up to four
+// K-steps ahead; the gathered rows mostly hit L2 and run three ahead.
 //
 // The same kernel, instantiated with kGather = false, is the grouped GEMM of
 // rows that are already in expert order (the down-projection that follows the
@@ -76,8 +77,16 @@ constexpr int ROW_BYTES = 128;               // bytes of one row segment per sta
 constexpr int B_BOX = 64;                    // W box: 64 columns (bf16) or 64 rows (FP8 codes)
 constexpr int B_BOX_BYTES = B_BOX * ROW_BYTES;  // 8 KiB
 constexpr int A_BYTES = BM * BK * 2;         // 16 KiB per m-tile
-constexpr int STAGES = 3;
-constexpr int STAGE_BYTES = 64 * 1024;       // W tile (bn_max*128 B) + m-tiles
+// Two rings, one slot per K-step each: the W ring runs up to four K-steps
+// ahead of the tensor cores (HBM latency), the A ring three (gathered rows).
+// A W slot holds the W tile (bn_max x 128 B); 3-m-tile units (bn_max = 128)
+// put their third A tile in its second half. An A slot holds m-tiles 0, 1.
+constexpr int W_STAGES = 4;
+constexpr int A_STAGES = 3;
+constexpr int W_SLOT = 32 * 1024;
+constexpr int A_SLOT = 2 * A_BYTES;
+constexpr int A_RING_OFF = W_STAGES * W_SLOT;                // 128 KiB
+constexpr int RING_BYTES = A_RING_OFF + A_STAGES * A_SLOT;   // 224 KiB
 constexpr int UMMA_K = 16;
 constexpr uint32_t TMEM_COLS = 512;
 
@@ -97,19 +106,33 @@ __device__ __forceinline__ int gather_index(int warp, int lane) {
 constexpr int ROWS_PER_PASS = GATHER_THREADS / 8;    // 8 threads per 128-byte row segment
 constexpr int ROWS_PER_THREAD = BM / ROWS_PER_PASS;  // per m-tile
 constexpr int MAX_MPU = 3;                   // m-tiles per unit
-constexpr int W_PREFETCH = 6;                // K-steps of W prefetched into L2 ahead of the loads
-
 struct Ctrl {
-    uint64_t full[STAGES];   // 1 arrive (W, + tx bytes) + one arrive per gather thread
-    uint64_t empty[STAGES];  // one tcgen05.commit
-    uint64_t acc_full;       // one tcgen05.commit per unit
-    uint64_t acc_empty;      // one arrive per epilogue warp
+    uint64_t wfull[W_STAGES];   // W producer arrive + tx bytes (+ one arrival per gather thread)
+    uint64_t wempty[W_STAGES];  // one tcgen05.commit
+    uint64_t afull[A_STAGES];   // one arrival per gather thread (grouped GEMM: W producer + tx)
+    uint64_t aempty[A_STAGES];  // one tcgen05.commit
+    uint64_t acc_full;          // one tcgen05.commit per unit
+    uint64_t acc_empty;         // one arrive per epilogue warp
     uint64_t drain;
     uint32_t tmem_base;
     int abort;
 };
 
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + static_cast<int>(sizeof(Ctrl)) + 64;
+constexpr int SMEM_BYTES = RING_BYTES + 1024 + static_cast<int>(sizeof(Ctrl)) + 64;
+static_assert(SMEM_BYTES <= 232448, "shared memory per block");
+
+// Slot index and phase parity of one ring, advanced once per K-step.
+template <int N>
+struct Cursor {
+    int s = 0;
+    uint32_t ph = 0;
+    __device__ __forceinline__ void next() {
+        if (++s == N) {
+            s = 0;
+            ph ^= 1u;
+        }
+    }
+};
 
 struct Unit {
     int e;        // expert
@@ -237,12 +260,12 @@ __global__ void __launch_bounds__(THREADS, 1)
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t sbase = (raw + 1023u) & ~1023u;
     uint8_t* base_ptr = smem_raw + (sbase - raw);
-    Ctrl* ctl = reinterpret_cast<Ctrl*>(base_ptr + STAGES * STAGE_BYTES);
+    Ctrl* ctl = reinterpret_cast<Ctrl*>(base_ptr + RING_BYTES);
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int R = T * k;
     constexpr int ELEM = kFp8 ? 1 : 2;              // bytes per element
-    constexpr int BKE = ROW_BYTES / ELEM;           // K elements per stage
+    constexpr int BKE = ROW_BYTES / ELEM;           // K elements per K-step
     constexpr int KCHUNK = 16 / ELEM;               // K elements per 16-byte chunk
     const int nk = (D + BKE - 1) / BKE;
     // FP8 blocked W: box (e, column block nb, K block kb) starts at row
@@ -251,18 +274,29 @@ __global__ void __launch_bounds__(THREADS, 1)
     auto fp8_box_row = [&](int e, int nb, int kb) {
         return ((e * nb_count + nb) * nk + kb) * B_BOX;
     };
+    // shared-memory address of m-tile mt of a K-step using W slot ws, A slot as
+    auto a_tile = [&](int ws, int as, int mt) -> uint32_t {
+        return mt < 2 ? sbase + A_RING_OFF + as * A_SLOT + mt * A_BYTES
+                      : sbase + ws * W_SLOT + (W_SLOT - A_BYTES);
+    };
 
-    const uint32_t full0 = smem_addr(&ctl->full[0]);
-    const uint32_t empty0 = smem_addr(&ctl->empty[0]);
+    const uint32_t wfull0 = smem_addr(&ctl->wfull[0]);
+    const uint32_t wempty0 = smem_addr(&ctl->wempty[0]);
+    const uint32_t afull0 = smem_addr(&ctl->afull[0]);
+    const uint32_t aempty0 = smem_addr(&ctl->aempty[0]);
     const uint32_t acc_full = smem_addr(&ctl->acc_full);
     const uint32_t acc_empty = smem_addr(&ctl->acc_empty);
     const uint32_t drain = smem_addr(&ctl->drain);
     volatile int* abort = &ctl->abort;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < STAGES; ++s) {
-            mbar_init(full0 + 8 * s, kGather ? 1 + GATHER_THREADS : 1);
-            mbar_init(empty0 + 8 * s, 1);
+        for (int s = 0; s < W_STAGES; ++s) {
+            mbar_init(wfull0 + 8 * s, kGather ? 1 + GATHER_THREADS : 1);
+            mbar_init(wempty0 + 8 * s, 1);
+        }
+        for (int s = 0; s < A_STAGES; ++s) {
+            mbar_init(afull0 + 8 * s, kGather ? GATHER_THREADS : 1);
+            mbar_init(aempty0 + 8 * s, 1);
         }
         mbar_init(acc_full, 1);
         mbar_init(acc_empty, EPI_WARPS);
@@ -294,8 +328,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         const uint64_t pol_x = policy_evict_last();  // rows are re-read by the unit's other n-tiles
         Walker wk;
         wk.init(offsets, E, R, De);
-        int stage = 0;
-        uint32_t phase = 0;
+        Cursor<W_STAGES> wc;
+        Cursor<A_STAGES> ac;
         bool ok = true, bad = false;
         for (int64_t u = blockIdx.x; ok; u += gridDim.x) {
             Unit U;
@@ -318,28 +352,30 @@ __global__ void __launch_bounds__(THREADS, 1)
                     }
                     src[mt][i] = p;
                 }
-            const uint32_t a_off = static_cast<uint32_t>(U.bn_max) * ROW_BYTES;
             for (int ks = 0; ks < nk; ++ks) {
-                if (!warp_wait(empty0 + 8 * stage, phase ^ 1u, abort, limit)) {
+                // A slot free means the MMAs of the K-step three back are
+                // done, and with them those of the K-step four back, the last
+                // user of this K-step's W slot (its second half may take m-tile 2).
+                if (!warp_wait(aempty0 + 8 * ac.s, ac.ph ^ 1u, abort, limit)) {
                     if (lane == 0) fail(abort, status);
                     ok = false;
                     break;
                 }
-                const uint32_t dst0 = sbase + stage * STAGE_BYTES + a_off + rb * 128 + swz;
                 const uint32_t nbytes = (ks * BKE + c * KCHUNK < D) ? 16u : 0u;
                 const int64_t koff = static_cast<int64_t>(ks) * ROW_BYTES;
 #pragma unroll
-                for (int mt = 0; mt < MAX_MPU; ++mt)
+                for (int mt = 0; mt < MAX_MPU; ++mt) {
+                    const uint32_t dst0 = a_tile(wc.s, ac.s, mt) + rb * 128 + swz;
 #pragma unroll
                     for (int i = 0; i < ROWS_PER_THREAD; ++i)
                         if (src[mt][i])
-                            cp_async_16(dst0 + mt * A_BYTES + i * (ROWS_PER_PASS * 128),
+                            cp_async_16(dst0 + i * (ROWS_PER_PASS * 128),
                                         nbytes ? src[mt][i] + koff : src[mt][i], nbytes, pol_x);
-                cp_async_arrive_noinc(full0 + 8 * stage);
-                if (++stage == STAGES) {
-                    stage = 0;
-                    phase ^= 1u;
                 }
+                cp_async_arrive_noinc(afull0 + 8 * ac.s);
+                cp_async_arrive_noinc(wfull0 + 8 * wc.s);
+                ac.next();
+                wc.next();
             }
         }
         // Copies still in flight must land before the CTA may exit.
@@ -350,76 +386,62 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (lane == 0) {
             const uint64_t pol_once = policy_evict_first();
             const uint64_t pol_reuse = policy_evict_last();  // also A: re-read by every n-tile
-            Walker wk, pf;
+            Walker wk;
             wk.init(offsets, E, R, De);
-            pf.init(offsets, E, R, De);
-            // Prefetch cursor: unit pf_u, K-step pf_ks, W_PREFETCH steps ahead.
-            int64_t pf_u = blockIdx.x;
-            int pf_ks = 0;
-            Unit PU;
-            bool pf_live = pf.find(pf_u, PU);
-            auto prefetch_one = [&]() {
-                if (!pf_live) return;
-                for (int b = 0; b < PU.bn / B_BOX; ++b) {
-                    if (kFp8)
-                        tma_prefetch_2d(&wmap, 0, fp8_box_row(PU.e, PU.n0 / B_BOX + b, pf_ks));
-                    else
-                        tma_prefetch_3d(&wmap, PU.n0 + b * B_BOX, pf_ks * BKE, PU.e);
-                }
-                if (++pf_ks == nk) {
-                    pf_ks = 0;
-                    pf_u += gridDim.x;
-                    pf_live = pf.find(pf_u, PU);
-                }
-            };
-            for (int i = 0; i < W_PREFETCH; ++i) prefetch_one();
-            int stage = 0;
-            uint32_t phase = 0, issued = 0, issued_par = 0;
+            Cursor<W_STAGES> wc;
+            Cursor<A_STAGES> ac;
+            uint32_t w_issued = 0, w_par = 0, a_issued = 0, a_par = 0;
             bool ok = true;
             for (int64_t u = blockIdx.x; ok; u += gridDim.x) {
                 Unit U;
                 if (!wk.find(u, U)) break;
                 const int nbox = U.bn / B_BOX;
                 const uint64_t pol = U.shared_w ? pol_reuse : pol_once;
-                const uint32_t a_off = static_cast<uint32_t>(U.bn_max) * ROW_BYTES;
-                const uint32_t tx = static_cast<uint32_t>(nbox * B_BOX_BYTES) +
-                                    (kGather ? 0u : static_cast<uint32_t>(U.mpu * A_BYTES));
+                // grouped GEMM: m-tiles 0, 1 to the A slot, m-tile 2 to the W slot
+                const int a_lo = U.mpu < 2 ? U.mpu : 2;
+                const uint32_t wtx = static_cast<uint32_t>(nbox * B_BOX_BYTES) +
+                                     (!kGather && U.mpu > 2 ? static_cast<uint32_t>(A_BYTES) : 0u);
+                const uint32_t atx = static_cast<uint32_t>(a_lo * A_BYTES);
                 for (int ks = 0; ks < nk; ++ks) {
-                    prefetch_one();
-                    if (!mbar_wait(empty0 + 8 * stage, phase ^ 1u, abort, limit)) {
+                    if (!mbar_wait(wempty0 + 8 * wc.s, wc.ph ^ 1u, abort, limit) ||
+                        (!kGather && !mbar_wait(aempty0 + 8 * ac.s, ac.ph ^ 1u, abort, limit))) {
                         fail(abort, status);
                         ok = false;
                         break;
                     }
-                    const uint32_t full = full0 + 8 * stage;
-                    mbar_arrive_expect_tx(full, tx);
-                    const uint32_t sb = sbase + stage * STAGE_BYTES;
+                    const uint32_t wfull = wfull0 + 8 * wc.s;
+                    mbar_arrive_expect_tx(wfull, wtx);
+                    const uint32_t wsl = sbase + wc.s * W_SLOT;
                     for (int b = 0; b < nbox; ++b) {
                         // bf16: 64 columns x 64 K rows (MN-major); FP8: 128 K codes x 64
                         // columns (K-major). Either way box b lands 8 KiB further.
                         if (kFp8)
-                            tma_load_2d(sb + b * B_BOX_BYTES, &wmap, 0,
-                                        fp8_box_row(U.e, U.n0 / B_BOX + b, ks), full, pol);
+                            tma_load_2d(wsl + b * B_BOX_BYTES, &wmap, 0,
+                                        fp8_box_row(U.e, U.n0 / B_BOX + b, ks), wfull, pol);
                         else
-                            tma_load_3d(sb + b * B_BOX_BYTES, &wmap, U.n0 + b * B_BOX, ks * BKE,
-                                        U.e, full, pol);
+                            tma_load_3d(wsl + b * B_BOX_BYTES, &wmap, U.n0 + b * B_BOX, ks * BKE,
+                                        U.e, wfull, pol);
                     }
-                    if (!kGather)  // rows past the expert's end are loaded but never stored
+                    w_issued |= 1u << wc.s;
+                    w_par = (w_par & ~(1u << wc.s)) | (wc.ph << wc.s);
+                    if (!kGather) {  // rows past the expert's end are loaded but never stored
+                        const uint32_t afull = afull0 + 8 * ac.s;
+                        mbar_arrive_expect_tx(afull, atx);
                         for (int mt = 0; mt < U.mpu; ++mt)
-                            tma_load_2d(sb + a_off + mt * A_BYTES, &amap, ks * BKE, U.row0 + mt * BM,
-                                        full, pol_reuse);
-                    issued |= 1u << stage;
-                    issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
-                    if (++stage == STAGES) {
-                        stage = 0;
-                        phase ^= 1u;
+                            tma_load_2d(a_tile(wc.s, ac.s, mt), &amap, ks * BKE, U.row0 + mt * BM,
+                                        mt < 2 ? afull : wfull, pol_reuse);
+                        a_issued |= 1u << ac.s;
+                        a_par = (a_par & ~(1u << ac.s)) | (ac.ph << ac.s);
                     }
+                    wc.next();
+                    ac.next();
                 }
             }
             // Every copy this thread started must land before the CTA may exit.
-            for (int s = 0; s < STAGES; ++s)
-                if ((issued >> s) & 1u)
-                    mbar_wait(full0 + 8 * s, (issued_par >> s) & 1u, nullptr, limit);
+            for (int s = 0; s < W_STAGES; ++s)
+                if ((w_issued >> s) & 1u) mbar_wait(wfull0 + 8 * s, (w_par >> s) & 1u, nullptr, limit);
+            for (int s = 0; s < A_STAGES; ++s)
+                if ((a_issued >> s) & 1u) mbar_wait(afull0 + 8 * s, (a_par >> s) & 1u, nullptr, limit);
         }
         __syncwarp();
     } else if (warp == MMA_WARP) {
@@ -427,9 +449,21 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (lane == 0) {
             Walker wk;
             wk.init(offsets, E, R, De);
-            int stage = 0;
-            uint32_t phase = 0, acc_phase = 0;
+            Cursor<W_STAGES> wc;
+            Cursor<A_STAGES> ac;
+            uint32_t acc_phase = 0;
             bool ok = true;
+            // Descriptors of shared-memory address 0 (the address field holds
+            // bytes >> 4, so an operand at byte offset o adds o >> 4).
+            // A: K-major, rows 128 B apart, 8-row groups 1024 B apart; a K step
+            // (16 bf16 or 32 FP8 elements) moves 32 B inside the swizzled row.
+            // B (bf16): MN-major (W rows are N-contiguous), 64-column blocks
+            // 8 KiB apart (LBO), 8-row K groups 1024 B apart (SBO); a K step of
+            // 16 rows is 2 KiB. B (FP8): K-major like A.
+            const uint64_t a_desc0 = sdesc_sw128(0, 16, 1024);
+            const uint64_t b_desc0 = kFp8 ? sdesc_sw128(0, 16, 1024)
+                                          : sdesc_sw128(0, B_BOX_BYTES, 1024);
+            constexpr uint32_t b_step = kFp8 ? (32 >> 4) : ((UMMA_K * 128) >> 4);
             for (int64_t u = blockIdx.x; ok; u += gridDim.x) {
                 Unit U;
                 if (!wk.find(u, U)) break;
@@ -440,23 +474,11 @@ __global__ void __launch_bounds__(THREADS, 1)
                 tc_fence_after_sync();
                 const uint32_t idesc =
                     kFp8 ? idesc_e4m3_f32(BM, U.bn) : idesc_bf16_f32(BM, U.bn, true);
-                // Descriptors of stage 0; a stage adds STAGE_BYTES, an m-tile
-                // A_BYTES, a K step of 16 adds 32 B (A, inside the swizzled
-                // row) or 16 rows = 2 KiB (B). The address field holds bytes >> 4.
-                // A: K-major, rows 128 B apart, 8-row groups 1024 B apart.
-                // B: MN-major (W rows are N-contiguous), 64-column blocks
-                // 8 KiB apart (LBO), 8-row K groups 1024 B apart (SBO).
-                // FP8: B is K-major like A (rows 128 B apart, 8-row groups 1024 B
-                // apart) and a K step of 32 codes moves 32 B inside the row.
-                const uint64_t a_desc0 =
-                    sdesc_sw128(sbase + static_cast<uint32_t>(U.bn_max) * ROW_BYTES, 16, 1024);
-                const uint64_t b_desc0 = kFp8 ? sdesc_sw128(sbase, 16, 1024)
-                                              : sdesc_sw128(sbase, B_BOX_BYTES, 1024);
-                constexpr uint32_t b_step = kFp8 ? (32 >> 4) : ((UMMA_K * 128) >> 4);
                 const int mpu = U.mpu;
                 const uint32_t acc_stride = static_cast<uint32_t>(U.bn_max);
                 for (int ks = 0; ks < nk; ++ks) {
-                    if (!mbar_wait(full0 + 8 * stage, phase, abort, limit)) {
+                    if (!mbar_wait(wfull0 + 8 * wc.s, wc.ph, abort, limit) ||
+                        !mbar_wait(afull0 + 8 * ac.s, ac.ph, abort, limit)) {
                         fail(abort, status);
                         ok = false;
                         break;
@@ -465,13 +487,12 @@ __global__ void __launch_bounds__(THREADS, 1)
                     // The gathered rows were written by cp.async (generic proxy);
                     // order them before the tensor cores' async-proxy reads.
                     fence_proxy_async_smem();
-                    const uint64_t sdelta = static_cast<uint64_t>(stage) * (STAGE_BYTES >> 4);
-                    const uint64_t a_st = a_desc0 + sdelta, b_st = b_desc0 + sdelta;
+                    const uint64_t b_st = b_desc0 + ((sbase + wc.s * W_SLOT) >> 4);
                     for (int mt = 0; mt < mpu; ++mt) {
-                        const uint64_t a_mt = a_st + static_cast<uint64_t>(mt) * (A_BYTES >> 4);
+                        const uint64_t a_mt = a_desc0 + (a_tile(wc.s, ac.s, mt) >> 4);
                         const uint32_t d = tmem + static_cast<uint32_t>(mt) * acc_stride;
 #pragma unroll
-                        for (int kk = 0; kk < 4; ++kk) {  // four K steps of 32 bytes per stage
+                        for (int kk = 0; kk < 4; ++kk) {  // four K steps of 32 bytes per K-step
                             if (kFp8)
                                 mma_f8(d, a_mt + kk * (32 >> 4), b_st + kk * b_step, idesc,
                                        (ks | kk) != 0 ? 1u : 0u);
@@ -480,11 +501,10 @@ __global__ void __launch_bounds__(THREADS, 1)
                                          (ks | kk) != 0 ? 1u : 0u);
                         }
                     }
-                    mma_commit(empty0 + 8 * stage);
-                    if (++stage == STAGES) {
-                        stage = 0;
-                        phase ^= 1u;
-                    }
+                    mma_commit(wempty0 + 8 * wc.s);
+                    mma_commit(aempty0 + 8 * ac.s);
+                    wc.next();
+                    ac.next();
                 }
                 if (!ok) break;
                 mma_commit(acc_full);

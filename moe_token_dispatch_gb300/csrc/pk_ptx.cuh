@@ -416,3 +416,22 @@ __device__ __forceinline__ void st_cluster_u32(uint32_t addr_cluster, uint32_t v
     asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr_cluster), "r"(v) : "memory");
 }
 }  // namespace pk
+
+namespace pk {
+// tma_prefetch_3d with an L2 eviction-priority policy for the prefetched lines.
+__device__ __forceinline__ void tma_prefetch_3d_hint(const CUtensorMap* map, int c0, int c1, int c2,
+                                                     uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.prefetch.tensor.3d.L2.global.tile.L2::cache_hint [%0, {%1, %2, %3}], %4;" ::"l"(
+            map),
+        "r"(c0), "r"(c1), "r"(c2), "l"(policy)
+        : "memory");
+}
+__device__ __forceinline__ void tma_prefetch_2d_hint(const CUtensorMap* map, int c0, int c1,
+                                                     uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.prefetch.tensor.2d.L2.global.tile.L2::cache_hint [%0, {%1, %2}], %3;" ::"l"(map),
+        "r"(c0), "r"(c1), "l"(policy)
+        : "memory");
+}
+}  // namespace pk
