@@ -212,40 +212,52 @@ __device__ __forceinline__ void fail(volatile int* abort, int32_t* status) {
     *abort = 1;
 }
 
+__device__ __forceinline__ uint32_t pack_bf16x2(uint32_t lo, uint32_t hi) {
+    __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(lo), __uint_as_float(hi));
+    return *reinterpret_cast<uint32_t*>(&b2);
+}
+
+// 32 fp32 accumulators of one row -> bf16 columns [col0, col0 + 32), those
+// below De. wide: 32-byte stores (row and column offsets 32-byte aligned),
+// so a warp's store instruction writes 32 whole sectors, else 16-byte ones.
 __device__ __forceinline__ void store_row_chunk(uint16_t* dst, const uint32_t (&v)[32], int col0,
-                                                int De) {
+                                                int De, bool wide) {
+    if (wide) {
+#pragma unroll
+        for (int g = 0; g < 2; ++g) {
+            if (col0 + g * 16 < De) {
+                uint32_t w[8];
+#pragma unroll
+                for (int h = 0; h < 8; ++h) w[h] = pack_bf16x2(v[g * 16 + 2 * h], v[g * 16 + 2 * h + 1]);
+                asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(
+                                 dst + col0 + g * 16),
+                             "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]),
+                             "r"(w[6]), "r"(w[7])
+                             : "memory");
+            }
+        }
+        return;
+    }
 #pragma unroll
     for (int g = 0; g < 4; ++g) {
         if (col0 + g * 8 < De) {
             uint4 pkd;
-            uint32_t* w = reinterpret_cast<uint32_t*>(&pkd);
-#pragma unroll
-            for (int h = 0; h < 4; ++h) {
-                __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(v[g * 8 + 2 * h]),
-                                                          __uint_as_float(v[g * 8 + 2 * h + 1]));
-                w[h] = *reinterpret_cast<uint32_t*>(&b2);
-            }
+            pkd.x = pack_bf16x2(v[g * 8 + 0], v[g * 8 + 1]);
+            pkd.y = pack_bf16x2(v[g * 8 + 2], v[g * 8 + 3]);
+            pkd.z = pack_bf16x2(v[g * 8 + 4], v[g * 8 + 5]);
+            pkd.w = pack_bf16x2(v[g * 8 + 6], v[g * 8 + 7]);
             *reinterpret_cast<uint4*>(dst + col0 + g * 8) = pkd;
         }
     }
 }
 
-// FP8 epilogue: accumulator x row scale x column scale (fp32), then bf16.
-__device__ __forceinline__ void store_row_chunk_scaled(uint16_t* dst, uint32_t (&v)[32], int col0,
-                                                       int De, float rs,
-                                                       const float* __restrict__ sw_e) {
+// FP8 epilogue: accumulator x row scale, then x column scale (fp32). Lane L
+// holds the scale of column col0 + L (`cs`); column j's is broadcast to the
+// whole warp by a shuffle, so every lane of the warp must call this.
+__device__ __forceinline__ void scale_chunk(uint32_t (&v)[32], float rs, float cs) {
 #pragma unroll
-    for (int g = 0; g < 4; ++g) {
-        if (col0 + g * 8 < De) {
-            const float4 s0 = __ldg(reinterpret_cast<const float4*>(sw_e + col0 + g * 8));
-            const float4 s1 = __ldg(reinterpret_cast<const float4*>(sw_e + col0 + g * 8 + 4));
-            const float sc[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
-#pragma unroll
-            for (int h = 0; h < 8; ++h)
-                v[g * 8 + h] = __float_as_uint(__uint_as_float(v[g * 8 + h]) * rs * sc[h]);
-        }
-    }
-    store_row_chunk(dst, v, col0, De);
+    for (int j = 0; j < 32; ++j)
+        v[j] = __float_as_uint((__uint_as_float(v[j]) * rs) * __shfl_sync(0xffffffffu, cs, j));
 }
 
 template <bool kGather, bool kFp8>
@@ -518,6 +530,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     } else if (warp < EPI_WARPS) {
         // ------------------------------------------------------ epilogue
         const int q = warp;  // TMEM lane quarter this warp may access (warps 0..3)
+        const bool wide = (De % 16) == 0 && (reinterpret_cast<uintptr_t>(out) & 31u) == 0;
         Walker wk;
         wk.init(offsets, E, R, De);
         uint32_t acc_phase = 0;
@@ -550,6 +563,13 @@ __global__ void __launch_bounds__(THREADS, 1)
                 const uint32_t tbase = tmem + (static_cast<uint32_t>(q * 32) << 16) +
                                        static_cast<uint32_t>(mt * U.bn_max);
                 for (int cc = 0; cc < U.bn / 32; cc += 2) {
+                    // FP8: this lane's column scales, loaded before the TMEM reads
+                    float cs0 = 0.0f, cs1 = 0.0f;
+                    if (kFp8) {
+                        const int ca = U.n0 + cc * 32 + lane, cb = ca + 32;
+                        if (ca < De) cs0 = __ldg(sw_e + ca);
+                        if (cb < De) cs1 = __ldg(sw_e + cb);
+                    }
                     uint32_t v0[32], v1[32];
                     tmem_ld_32x32b_x32(tbase + cc * 32, v0);
                     tmem_ld_32x32b_x32(tbase + cc * 32 + 32, v1);
@@ -560,14 +580,13 @@ __global__ void __launch_bounds__(THREADS, 1)
                         if (lane == 0) mbar_arrive(acc_empty);
                         released = true;
                     }
+                    if (kFp8) {  // all lanes: the scales travel by shuffles
+                        scale_chunk(v0, rs, cs0);
+                        scale_chunk(v1, rs, cs1);
+                    }
                     if (valid) {
-                        if (kFp8) {
-                            store_row_chunk_scaled(orow, v0, U.n0 + cc * 32, De, rs, sw_e);
-                            store_row_chunk_scaled(orow, v1, U.n0 + cc * 32 + 32, De, rs, sw_e);
-                        } else {
-                            store_row_chunk(orow, v0, U.n0 + cc * 32, De);
-                            store_row_chunk(orow, v1, U.n0 + cc * 32 + 32, De);
-                        }
+                        store_row_chunk(orow, v0, U.n0 + cc * 32, De, wide);
+                        store_row_chunk(orow, v1, U.n0 + cc * 32 + 32, De, wide);
                     }
                 }
             }
