@@ -418,7 +418,7 @@ def run_ours(args, wl):
                 "note": "x and topk_idx copied in from pinned host memory and out copied back "
                         "every step, copies of neighbouring steps overlapped with compute on "
                         "three streams; W stays resident (layer weights)"},
-        "gpu_launches": 4 * K,
+        "gpu_launches": (pk.pk_moe_route_kernel_launches(wl.T, wl.k, wl.E) + 1) * K,
         "clocks": sampler.summary(wall0, wall1) if sampler else None,
     }
     return line

@@ -265,6 +265,14 @@ int pk_moe_route_noalloc(const int32_t* topk_idx, int32_t T, int32_t k, int32_t 
                          int32_t* inv_perm, int32_t* status_word, void* stream);
 
 /*
+ * Number of kernels that pk_moe_route_counts followed by pk_moe_build_perm
+ * launch for these sizes (host arithmetic, no CUDA call): 2 when every
+ * 2048-entry chunk histogram fits one block's shared memory (counts and scan
+ * in one kernel, then the permutation), else 3. -1 for invalid sizes.
+ */
+int pk_moe_route_kernel_launches(int32_t T, int32_t k, int32_t E);
+
+/*
  * Kernel used by pk_moe_dispatch_gemm and pk_moe_dispatch_gemm_fp8 for
  * later calls from this process (both compute the same result, within
  * fp32 summation order):

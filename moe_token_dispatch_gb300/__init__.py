@@ -34,6 +34,7 @@ from ._binding import (  # noqa: F401
     pk_moe_quant_rows,
     pk_moe_quant_weights,
     pk_moe_route_counts,
+    pk_moe_route_kernel_launches,
     pk_moe_route_noalloc,
     pk_moe_router_topk,
     pk_moe_set_gemm_kernel,

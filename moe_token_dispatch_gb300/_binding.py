@@ -68,6 +68,8 @@ def _load():
     lib.pk_moe_router_topk.argtypes = [P, I32, I32, I32, P, P, P]
     lib.pk_moe_combine.restype = ctypes.c_int
     lib.pk_moe_combine.argtypes = [P, P, P, I32, I32, I32, P, P, P]
+    lib.pk_moe_route_kernel_launches.restype = ctypes.c_int
+    lib.pk_moe_route_kernel_launches.argtypes = [I32, I32, I32]
     lib.pk_moe_set_gemm_kernel.restype = ctypes.c_int
     lib.pk_moe_set_gemm_kernel.argtypes = [ctypes.c_int]
     lib.pk_moe_set_wait_limit_ns.restype = None
@@ -271,6 +273,10 @@ def pk_moe_route_noalloc(topk_idx: torch.Tensor, E: int, expert_offsets: torch.T
         _ptr(inv_perm, torch.int32, "inv_perm", T * k),
         _ptr(status_word, torch.int32, "status_word", 1), _stream(stream))
     _check(rc, "pk_moe_route_noalloc")
+
+
+def pk_moe_route_kernel_launches(T: int, k: int, E: int) -> int:
+    return int(lib.pk_moe_route_kernel_launches(T, k, E))
 
 
 def pk_moe_set_gemm_kernel(kernel: int) -> None:

@@ -186,6 +186,11 @@ int pk_moe_combine(const uint16_t* src, const int32_t* inv_perm, const float* ga
     return err == cudaSuccess ? PK_OK : PK_ERR_CUDA;
 }
 
+int pk_moe_route_kernel_launches(int32_t T, int32_t k, int32_t E) {
+    if (T < 0 || k < 1 || E < 1) return -1;
+    return pk::route_kernel_launches(static_cast<int64_t>(T) * k, E);
+}
+
 int pk_moe_set_gemm_kernel(int kernel) {
     if (kernel != PK_GEMM_KERNEL_AUTO && kernel != PK_GEMM_KERNEL_SINGLE &&
         kernel != PK_GEMM_KERNEL_PAIR)

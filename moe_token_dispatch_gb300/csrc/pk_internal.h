@@ -19,6 +19,8 @@ inline int route_blocks(int64_t R) { return static_cast<int>((R + kRouteChunk - 
 cudaError_t launch_route_counts(const int32_t* topk, int32_t R, int32_t E, int32_t* counts,
                                 int32_t* offsets, int32_t* blockbase, int32_t* status,
                                 cudaStream_t stream);
+// Kernels launched by launch_route_counts + launch_build_perm for R entries.
+int route_kernel_launches(int64_t R, int32_t E);
 cudaError_t launch_build_perm(const int32_t* topk, int32_t R, int32_t E,
                               const int32_t* blockbase, int32_t* perm, int32_t* inv_perm,
                               int32_t* status, cudaStream_t stream);

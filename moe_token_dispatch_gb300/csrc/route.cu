@@ -11,8 +11,12 @@
 //                  row b rewritten in place to the first output position of
 //                  chunk b's entries of each expert:
 //                    base[b][e] = offsets[e] + sum_{b' < b} hist[b'][e];
-//   k_build_perm   each warp of block b owns a contiguous run of the chunk;
-//                  a per-warp histogram and a scan over warps give every warp
+//   k_route_small  both of the above in one block of 1024 threads, used when
+//                  every chunk histogram fits in its shared memory (one launch
+//                  instead of two for routing arrays up to ~10^5 entries);
+//   k_build_perm   each warp of block b owns a contiguous run of the chunk
+//                  (8 entries per lane, loaded once into registers); a
+//                  per-warp histogram and a scan over warps give every warp
 //                  its first position per expert, then warps walk their runs
 //                  32 entries at a time and rank equal experts inside a warp
 //                  with __match_any_sync. Positions follow flat order, so the
@@ -117,6 +121,95 @@ __global__ void __launch_bounds__(kScanThreads)
     }
 }
 
+// Exclusive scan of v[0, n) into out[0, n) by one block of kScanThreads
+// threads (each thread a run of consecutive values, a warp shuffle scan and a
+// scan of the 32 warp sums); returns the total to every thread. wsum: [32].
+__device__ int32_t block_exclusive_scan(const int32_t* v, int32_t* out, int n, int32_t* wsum) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int per = (n + kScanThreads - 1) / kScanThreads;
+    const int b0 = min(tid * per, n), b1 = min(b0 + per, n);
+    int32_t local = 0;
+    for (int i = b0; i < b1; ++i) local += v[i];
+    int32_t incl = local;
+    for (int d = 1; d < 32; d <<= 1) {
+        const int32_t t = __shfl_up_sync(0xffffffffu, incl, d);
+        if (lane >= d) incl += t;
+    }
+    if (lane == 31) wsum[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        int32_t w = wsum[lane];
+        for (int d = 1; d < 32; d <<= 1) {
+            const int32_t t = __shfl_up_sync(0xffffffffu, w, d);
+            if (lane >= d) w += t;
+        }
+        wsum[lane] = w;
+    }
+    __syncthreads();
+    int32_t run = (warp > 0 ? wsum[warp - 1] : 0) + incl - local;
+    for (int i = b0; i < b1; ++i) {
+        out[i] = run;
+        run += v[i];
+    }
+    const int32_t total = wsum[31];
+    __syncthreads();
+    return total;
+}
+
+// Chunk histograms, counts, offsets and chunk starting positions in one block.
+// Shared memory: hist [nblk][E], tot [E], offs [E], wsum [32].
+__global__ void __launch_bounds__(kScanThreads)
+    k_route_small(const int32_t* __restrict__ topk, int32_t R, int32_t E, int32_t nblk,
+                  int32_t* __restrict__ blockbase, int32_t* counts, int32_t* __restrict__ offsets,
+                  int32_t* status) {
+    extern __shared__ int32_t sm[];
+    int32_t* hist = sm;
+    int32_t* tot = hist + static_cast<int64_t>(nblk) * E;
+    int32_t* offs = tot + E;
+    int32_t* wsum = offs + E;
+    const uint32_t lane = threadIdx.x & 31;
+    for (int i = threadIdx.x; i < nblk * E; i += blockDim.x) hist[i] = 0;
+    __syncthreads();
+    bool bad = false;
+    // 32 consecutive entries always lie in one chunk (kRouteChunk % 32 == 0)
+    for (int base = 0; base < R; base += blockDim.x) {
+        const int i = base + threadIdx.x;
+        int32_t e = -1;
+        if (i < R) {
+            e = __ldg(topk + i);
+            if (e < 0 || e >= E) {
+                bad = true;
+                e = -1;
+            }
+        }
+        const uint32_t peers = __match_any_sync(0xffffffffu, e);
+        if (e >= 0 && lane == static_cast<uint32_t>(__ffs(peers) - 1))
+            atomicAdd(&hist[(i / kRouteChunk) * E + e], __popc(peers));
+    }
+    if (bad) report(status, PK_ERR_BAD_INDEX);
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        int32_t s = 0;
+        for (int b = 0; b < nblk; ++b) s += hist[b * E + e];
+        tot[e] = s;
+        if (counts) counts[e] = s;
+    }
+    __syncthreads();
+    const int32_t total = block_exclusive_scan(tot, offs, E, wsum);
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        offsets[e] = offs[e];
+        int32_t r = offs[e];
+        for (int b = 0; b < nblk; ++b) {
+            blockbase[static_cast<int64_t>(b) * E + e] = r;
+            r += hist[b * E + e];
+        }
+    }
+    if (threadIdx.x == 0) offsets[E] = total;
+}
+
+// Largest shared memory k_route_small may use (its histograms: nblk * E ints).
+constexpr size_t kRouteSmallSmem = 96 * 1024;
+
 __global__ void __launch_bounds__(kRouteThreads)
     k_build_perm(const int32_t* __restrict__ topk, int32_t R, int32_t E,
                  const int32_t* __restrict__ blockbase, int32_t* __restrict__ perm,
@@ -133,14 +226,24 @@ __global__ void __launch_bounds__(kRouteThreads)
     const int64_t wend = min(wbeg + kPerWarp, static_cast<int64_t>(R));
     int32_t* my = wpos + warp * E;
 
-    // Pass 1: histogram of this warp's run.
-    for (int64_t base = wbeg; base < wbeg + kPerWarp; base += 32) {
-        const int64_t i = base + lane;
+    // This lane's entries of the warp's run, loaded once (-1: none or invalid).
+    constexpr int kIter = kPerWarp / 32;
+    int32_t ent[kIter];
+#pragma unroll
+    for (int it = 0; it < kIter; ++it) {
+        const int64_t i = wbeg + it * 32 + lane;
         int32_t e = -1;
         if (i < wend) {
             e = __ldg(topk + i);
             if (e < 0 || e >= E) e = -1;
         }
+        ent[it] = e;
+    }
+
+    // Pass 1: histogram of this warp's run.
+#pragma unroll
+    for (int it = 0; it < kIter; ++it) {
+        const int32_t e = ent[it];
         const uint32_t peers = __match_any_sync(0xffffffffu, e);
         if (e >= 0 && lane == __ffs(peers) - 1) my[e] += __popc(peers);
         __syncwarp();
@@ -161,13 +264,10 @@ __global__ void __launch_bounds__(kRouteThreads)
 
     // Pass 3: scatter in flat order.
     bool bad = false;
-    for (int64_t base = wbeg; base < wbeg + kPerWarp; base += 32) {
-        const int64_t i = base + lane;
-        int32_t e = -1;
-        if (i < wend) {
-            e = __ldg(topk + i);
-            if (e < 0 || e >= E) e = -1;
-        }
+#pragma unroll
+    for (int it = 0; it < kIter; ++it) {
+        const int64_t i = wbeg + it * 32 + lane;
+        const int32_t e = ent[it];
         const uint32_t peers = __match_any_sync(0xffffffffu, e);
         if (e >= 0) {
             const int32_t pos = my[e] + __popc(peers & lt_mask);
@@ -187,12 +287,28 @@ __global__ void __launch_bounds__(kRouteThreads)
 
 namespace {
 int g_perm_smem_set[64] = {0};
+int g_small_smem_set[64] = {0};
 }
 
 cudaError_t launch_route_counts(const int32_t* topk, int32_t R, int32_t E, int32_t* counts,
                                 int32_t* offsets, int32_t* blockbase, int32_t* status,
                                 cudaStream_t stream) {
     const int nblk = route_blocks(R);
+    const size_t small_smem = sizeof(int32_t) * (static_cast<size_t>(nblk) * E + 2 * E + 32);
+    if (nblk > 0 && small_smem <= kRouteSmallSmem) {
+        int dev = 0;
+        cudaError_t err = cudaGetDevice(&dev);
+        if (err != cudaSuccess) return err;
+        if (small_smem > 48 * 1024 && (dev < 0 || dev >= 64 || !g_small_smem_set[dev])) {
+            err = cudaFuncSetAttribute(k_route_small, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(kRouteSmallSmem));
+            if (err != cudaSuccess) return err;
+            if (dev >= 0 && dev < 64) g_small_smem_set[dev] = 1;
+        }
+        k_route_small<<<1, kScanThreads, small_smem, stream>>>(topk, R, E, nblk, blockbase, counts,
+                                                               offsets, status);
+        return cudaGetLastError();
+    }
     if (nblk > 0) {
         k_route_hist<<<nblk, kRouteThreads, sizeof(int32_t) * E, stream>>>(topk, R, E, blockbase,
                                                                            status);
@@ -202,6 +318,13 @@ cudaError_t launch_route_counts(const int32_t* topk, int32_t R, int32_t E, int32
     k_route_scan<<<1, kScanThreads, sizeof(int32_t) * (2 * E + 32), stream>>>(blockbase, nblk, E,
                                                                              counts, offsets);
     return cudaGetLastError();
+}
+
+int route_kernel_launches(int64_t R, int32_t E) {
+    if (R <= 0) return 1;  // the scan alone writes the zero offsets
+    const int nblk = route_blocks(R);
+    const size_t small_smem = sizeof(int32_t) * (static_cast<size_t>(nblk) * E + 2 * E + 32);
+    return small_smem <= kRouteSmallSmem ? 2 : 3;
 }
 
 cudaError_t launch_build_perm(const int32_t* topk, int32_t R, int32_t E,

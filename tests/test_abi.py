@@ -144,3 +144,12 @@ def test_set_gemm_kernel(lib):
     assert L.pk_moe_set_gemm_kernel(-1) == 1
     for v in (1, 2, 0):
         assert L.pk_moe_set_gemm_kernel(v) == 0
+
+
+def test_route_kernel_launches(lib):
+    L = _raw(lib)
+    assert L.pk_moe_route_kernel_launches(8192, 8, 256) == 2     # 32 chunks x 256 experts
+    assert L.pk_moe_route_kernel_launches(12288, 8, 256) == 2    # 48 chunks: 51 KB of histograms
+    assert L.pk_moe_route_kernel_launches(2048, 8, 4096) == 3    # 8 chunks x 4096 experts: 128 KiB
+    assert L.pk_moe_route_kernel_launches(0, 8, 256) == 1
+    assert L.pk_moe_route_kernel_launches(-1, 8, 256) == -1

@@ -78,6 +78,27 @@ def test_skewed_routing_small(gpu_lib, gemm_kernel):
     check_case(gpu_lib, x, topk, W, 32)
 
 
+@pytest.mark.parametrize("T,k,E", [
+    (2048, 8, 4096),    # 8 chunks x 4096 experts: three kernels (histogram, scan, permutation)
+    (12288, 8, 256),    # 48 chunks: one-block counts + scan with 51 KB of shared memory
+    (100, 3, 7),        # one ragged chunk
+])
+def test_routing_kernel_paths(gpu_lib, T, k, E):
+    pk = gpu_lib
+    rng = np.random.default_rng(T + E)
+    topk = rng.integers(0, E, size=(T, k)).astype(np.int32)
+    md = pk.MoeDispatch(T, k, E, 64, 64)
+    md.route(torch.from_numpy(topk).cuda())
+    torch.cuda.synchronize()
+    assert md.status_code() == 0
+    ref = oracle.run(topk, E)
+    R = T * k
+    assert np.array_equal(md.counts.cpu().numpy().astype(np.int64), ref["counts"])
+    assert np.array_equal(md.offsets.cpu().numpy().astype(np.int64), ref["offsets"])
+    assert np.array_equal(md.perm[:R].cpu().numpy().astype(np.int64), ref["perm"])
+    assert np.array_equal(md.inv_perm[:R].cpu().numpy().astype(np.int64), ref["inv_perm"])
+
+
 def test_zero_tokens(gpu_lib):
     pk = gpu_lib
     md = pk.MoeDispatch(0, 2, 8, 64, 64)
