@@ -266,9 +266,9 @@ int pk_moe_route_noalloc(const int32_t* topk_idx, int32_t T, int32_t k, int32_t 
 
 /*
  * Number of kernels that pk_moe_route_counts followed by pk_moe_build_perm
- * launch for these sizes (host arithmetic, no CUDA call): 2 when every
- * 2048-entry chunk histogram fits one block's shared memory (counts and scan
- * in one kernel, then the permutation), else 3. -1 for invalid sizes.
+ * launch for these sizes (host arithmetic, no CUDA call): 2 when T*k is at
+ * most 4096 (counts and scan in one kernel, then the permutation), else 3
+ * (histogram, scan, permutation). -1 for invalid sizes.
  */
 int pk_moe_route_kernel_launches(int32_t T, int32_t k, int32_t E);
 

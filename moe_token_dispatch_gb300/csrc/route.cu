@@ -11,9 +11,10 @@
 //                  row b rewritten in place to the first output position of
 //                  chunk b's entries of each expert:
 //                    base[b][e] = offsets[e] + sum_{b' < b} hist[b'][e];
-//   k_route_small  both of the above in one block of 1024 threads, used when
-//                  every chunk histogram fits in its shared memory (one launch
-//                  instead of two for routing arrays up to ~10^5 entries);
+//   k_route_small  both of the above in one block of 1024 threads, for
+//                  routing arrays of at most two chunks (one launch instead
+//                  of two; on larger arrays one SM's __match_any_sync rate
+//                  makes it slower than the spread-out histogram);
 //   k_build_perm   each warp of block b owns a contiguous run of the chunk
 //                  (8 entries per lane, loaded once into registers); a
 //                  per-warp histogram and a scan over warps give every warp
@@ -207,7 +208,9 @@ __global__ void __launch_bounds__(kScanThreads)
     if (threadIdx.x == 0) offsets[E] = total;
 }
 
-// Largest shared memory k_route_small may use (its histograms: nblk * E ints).
+// k_route_small takes routing arrays of at most this many chunks whose
+// histograms (nblk * E ints) fit this much shared memory.
+constexpr int kRouteSmallChunks = 2;
 constexpr size_t kRouteSmallSmem = 96 * 1024;
 
 __global__ void __launch_bounds__(kRouteThreads)
@@ -295,7 +298,7 @@ cudaError_t launch_route_counts(const int32_t* topk, int32_t R, int32_t E, int32
                                 cudaStream_t stream) {
     const int nblk = route_blocks(R);
     const size_t small_smem = sizeof(int32_t) * (static_cast<size_t>(nblk) * E + 2 * E + 32);
-    if (nblk > 0 && small_smem <= kRouteSmallSmem) {
+    if (nblk > 0 && nblk <= kRouteSmallChunks && small_smem <= kRouteSmallSmem) {
         int dev = 0;
         cudaError_t err = cudaGetDevice(&dev);
         if (err != cudaSuccess) return err;
@@ -324,7 +327,7 @@ int route_kernel_launches(int64_t R, int32_t E) {
     if (R <= 0) return 1;  // the scan alone writes the zero offsets
     const int nblk = route_blocks(R);
     const size_t small_smem = sizeof(int32_t) * (static_cast<size_t>(nblk) * E + 2 * E + 32);
-    return small_smem <= kRouteSmallSmem ? 2 : 3;
+    return nblk <= kRouteSmallChunks && small_smem <= kRouteSmallSmem ? 2 : 3;
 }
 
 cudaError_t launch_build_perm(const int32_t* topk, int32_t R, int32_t E,

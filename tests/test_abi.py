@@ -148,8 +148,9 @@ def test_set_gemm_kernel(lib):
 
 def test_route_kernel_launches(lib):
     L = _raw(lib)
-    assert L.pk_moe_route_kernel_launches(8192, 8, 256) == 2     # 32 chunks x 256 experts
-    assert L.pk_moe_route_kernel_launches(12288, 8, 256) == 2    # 48 chunks: 51 KB of histograms
-    assert L.pk_moe_route_kernel_launches(2048, 8, 4096) == 3    # 8 chunks x 4096 experts: 128 KiB
+    assert L.pk_moe_route_kernel_launches(128, 8, 256) == 2      # one chunk
+    assert L.pk_moe_route_kernel_launches(512, 8, 4096) == 2     # two chunks x 4096 experts
+    assert L.pk_moe_route_kernel_launches(513, 8, 256) == 3      # three chunks
+    assert L.pk_moe_route_kernel_launches(8192, 8, 256) == 3
     assert L.pk_moe_route_kernel_launches(0, 8, 256) == 1
     assert L.pk_moe_route_kernel_launches(-1, 8, 256) == -1

@@ -80,7 +80,7 @@ def test_skewed_routing_small(gpu_lib, gemm_kernel):
 
 @pytest.mark.parametrize("T,k,E", [
     (2048, 8, 4096),    # 8 chunks x 4096 experts: three kernels (histogram, scan, permutation)
-    (12288, 8, 256),    # 48 chunks: one-block counts + scan with 51 KB of shared memory
+    (512, 8, 4096),     # two chunks x 4096 experts: one-block counts + scan, 64 KiB of shared memory
     (100, 3, 7),        # one ragged chunk
 ])
 def test_routing_kernel_paths(gpu_lib, T, k, E):
