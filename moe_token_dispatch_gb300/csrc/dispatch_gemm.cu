@@ -87,6 +87,12 @@ constexpr int W_SLOT = 32 * 1024;
 constexpr int A_SLOT = 2 * A_BYTES;
 constexpr int A_RING_OFF = W_STAGES * W_SLOT;                // 128 KiB
 constexpr int RING_BYTES = A_RING_OFF + A_STAGES * A_SLOT;   // 224 KiB
+// A gather thread infers from "its A slot is free" (the MMAs A_STAGES K-steps
+// back are done) that the W slot of the same K-step is free too (its last
+// user is W_STAGES K-steps back); that holds only with at least as many W
+// slots as A slots. Fewer would let the third A tile and the gather's
+// arrivals reach a W slot whose previous phase is still in use.
+static_assert(W_STAGES >= A_STAGES, "the A ring may not run further ahead than the W ring");
 constexpr int UMMA_K = 16;
 constexpr uint32_t TMEM_COLS = 512;
 
