@@ -209,3 +209,59 @@ def test_fp8_full_size_ep_sampled(gpu_lib):
     got = bf16_dev_to_f64(out[torch.from_numpy(rows).cuda()])
     assert_gemm_close(got, want, rows)
     assert bool(torch.isfinite(out.float()).all())
+
+
+def test_fp8_tiny_and_mid_workloads(gpu_lib):
+    """The named small workloads: every row of tiny, boundary and random rows of mid."""
+    c = ig.make_case(ig.WORKLOADS["tiny"])
+    _fp8_case(gpu_lib, c.x, c.topk, c.W, ig.WORKLOADS["tiny"].E)
+    wl = ig.WORKLOADS["mid"]
+    c = ig.make_case(wl)
+    rows = boundary_rows(oracle.route_counts(c.topk, wl.E)[1], np.random.default_rng(5), 256)
+    _fp8_case(gpu_lib, c.x, c.topk, c.W, wl.E, rows=rows)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", ["skew", "decode"])
+def test_fp8_full_size_sampled(gpu_lib, name):
+    """T=8192 (skew, Zipf-biased routing) or T=128 (decode), D=7168, E=256,
+    k=8, D_expert=2048: x codes bit-exact in full, W codes of a sample of
+    experts bit-exact, GEMM rows of those experts against the oracle."""
+    pk = gpu_lib
+    wl = ig.WORKLOADS[name]
+    x = ig.make_x(wl)
+    topk = ig.make_topk(wl)
+    ref = oracle.run(topk, wl.E)
+    counts = ref["counts"]
+    touched = np.flatnonzero(counts)
+    # the heaviest expert, the lightest touched ones, and a few in between
+    order = touched[np.argsort(counts[touched])]
+    experts = sorted({int(e) for e in list(order[:2]) + list(order[-2:]) +
+                      list(order[len(order) // 2:][:2])})
+    W = ig.make_W(wl, experts=experts)
+    md = pk.MoeDispatch(wl.T, wl.k, wl.E, wl.D, wl.De)
+    md.route(torch.from_numpy(topk).cuda())
+    xq_g, sx_g = _gpu_quant_rows(pk, x)
+    xq, sx = oracle.quant_rows(x)
+    assert np.array_equal(xq_g.cpu().numpy(), xq) and np.array_equal(sx_g.cpu().numpy(), sx)
+    Wd = u16_to_bf16_dev(W)
+    wq_g, sw_g = _gpu_quant_weights(pk, Wd)
+    del Wd
+    q_ref, s_ref = oracle.quant_cols(W[experts])
+    assert np.array_equal(wq_g[experts].cpu().numpy(), to_blocked(q_ref))
+    assert np.array_equal(sw_g[experts].cpu().numpy(), s_ref)
+    out = torch.empty((wl.T * wl.k, wl.De), dtype=torch.bfloat16, device="cuda")
+    pk.pk_moe_dispatch_gemm_fp8(xq_g, sx_g, md.perm, md.offsets, wq_g, sw_g, wl.k, out, md.status)
+    torch.cuda.synchronize()
+    assert md.status_code() == 0
+    offsets = ref["offsets"]
+    rows = boundary_rows(offsets, np.random.default_rng(6), 0)
+    rows = rows[np.isin(np.searchsorted(offsets, rows, side="right") - 1, experts)]
+    assert rows.size >= 6
+    wq_full = np.zeros((wl.E, wl.De, wl.D), dtype=np.uint8)
+    sw_full = np.ones((wl.E, wl.De), dtype=np.float32)
+    wq_full[experts] = q_ref
+    sw_full[experts] = s_ref
+    want = oracle.gemm_fp8_rows(xq, sx, ref["perm"], offsets, wq_full, sw_full, wl.k, rows)
+    got = bf16_dev_to_f64(out[torch.from_numpy(rows).cuda()])
+    assert_gemm_close(got, want, rows)
