@@ -99,6 +99,16 @@ def test_routing_kernel_paths(gpu_lib, T, k, E):
     assert np.array_equal(md.inv_perm[:R].cpu().numpy().astype(np.int64), ref["inv_perm"])
 
 
+def test_maximum_expert_count(gpu_lib, gemm_kernel):
+    """E = PK_MAX_EXPERTS (4096): three routing kernels, ~4 rows per expert,
+    thousands of one-m-tile units, every row of the GEMM checked."""
+    pk = gpu_lib
+    E = pk.PK_MAX_EXPERTS
+    x, topk, W = _case(2048, 64, E, 8, 64, seed=3)
+    assert pk.pk_moe_route_kernel_launches(2048, 8, E) == 3
+    check_case(pk, x, topk, W, E)
+
+
 def test_zero_tokens(gpu_lib):
     pk = gpu_lib
     md = pk.MoeDispatch(0, 2, 8, 64, 64)
