@@ -109,6 +109,37 @@ def test_maximum_expert_count(gpu_lib, gemm_kernel):
     check_case(pk, x, topk, W, E)
 
 
+def test_every_token_to_every_expert(gpu_lib, gemm_kernel):
+    """k = E: each expert receives all T tokens, in token order."""
+    T, D, E, De = 300, 128, 4, 192
+    x, _, W = _case(T, D, E, E, De, seed=4)
+    topk = np.stack([np.random.default_rng(t).permutation(E) for t in range(T)]).astype(np.int32)
+    res, ref = check_case(gpu_lib, x, topk, W, E)
+    assert res["counts"].tolist() == [T] * E
+
+
+def test_nan_input_row_propagates_only_to_its_rows(gpu_lib, gemm_kernel):
+    """IEEE propagation, no checks: a NaN in token t's row makes exactly the
+    output rows gathered from t NaN; every other row stays finite and within
+    tolerance of the oracle."""
+    T, D, E, k, De = 200, 256, 8, 2, 256
+    x, topk, W = _case(T, D, E, k, De, seed=8)
+    bad_t = 17
+    x = x.copy()
+    x[bad_t, 5] = 0x7FC0  # bf16 quiet NaN
+    res = run_gpu(gpu_lib, x, topk, u16_to_bf16_dev(W), E, De)
+    assert res["status"] == 0
+    out = bf16_dev_to_f64(res["out_dev"])
+    from_bad = (res["perm"] // k) == bad_t
+    assert from_bad.sum() == k
+    assert np.isnan(out[from_bad]).all()
+    assert np.isfinite(out[~from_bad]).all()
+    ref = oracle.run(topk, E)
+    rows = np.flatnonzero(~from_bad)
+    want = oracle.gemm_rows(x, ref["perm"], ref["offsets"], W, k, rows)
+    assert_gemm_close(out[rows], want, rows)
+
+
 def test_zero_tokens(gpu_lib):
     pk = gpu_lib
     md = pk.MoeDispatch(0, 2, 8, 64, 64)
