@@ -1,5 +1,5 @@
 // Inline-PTX building blocks for sm_103a: shared-memory barriers, TMA bulk
-// tensor copies (tiled and four-row gather), tcgen05 tensor-core MMAs with
+// tensor copies and L2 prefetches, tcgen05 tensor-core MMAs with
 // accumulators in tensor memory (TMEM), and the shared-memory matrix
 // descriptors they read. Written from the PTX ISA (tcgen05, cp.async.bulk.tensor,
 // mbarrier chapters); no library code.
@@ -92,17 +92,6 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
         "cp.async.bulk.tensor.3d.shared::cta.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
         " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
         "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(bar), "l"(policy)
-        : "memory");
-}
-
-// Four-row gather: rows r0..r3 of a 2-D tensor, columns [col, col + box
-// width), into four consecutive rows of shared memory (swizzled by the map).
-__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* map, int col, int r0,
-                                            int r1, int r2, int r3, uint32_t bar, uint64_t policy) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cta.global.tile::gather4.mbarrier::complete_tx::bytes"
-        ".L2::cache_hint [%0], [%1, {%2, %3, %4, %5, %6}], [%7], %8;" ::"r"(dst),
-        "l"(map), "r"(col), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(bar), "l"(policy)
         : "memory");
 }
 
@@ -236,23 +225,11 @@ __device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
 __device__ __forceinline__ void cp_async_wait_all() {
     asm volatile("cp.async.wait_all;" ::: "memory");
 }
-__device__ __forceinline__ void cp_async_commit() {
-    asm volatile("cp.async.commit_group;" ::: "memory");
-}
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
 // Orders generic-proxy shared-memory writes that this thread has observed
 // (its own, or others' through a barrier it waited on) before its later
 // async-proxy operations (tensor-core operand reads).
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-__device__ __forceinline__ uint64_t policy_evict_normal() {
-    uint64_t p;
-    asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
-    return p;
 }
 
 }  // namespace pk
@@ -274,27 +251,6 @@ __device__ __forceinline__ uint32_t map_to_cta(uint32_t saddr, uint32_t rank) {
 __device__ __forceinline__ void cluster_sync() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" :::
                      "memory");
-}
-// Bulk copy of `bytes` (multiple of 16) from this CTA's shared memory to a
-// cluster peer's; completion is counted in bytes on the peer's barrier.
-__device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst_cluster, uint32_t src_cta,
-                                                  uint32_t bytes, uint32_t bar_cluster) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-        ::"r"(dst_cluster), "r"(src_cta), "r"(bytes), "r"(bar_cluster)
-        : "memory");
-}
-__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void bulk_wait_read_all() {
-    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-}
-// Like mma_commit, but arrives on the barrier at the same offset in every CTA
-// of `cta_mask`.
-__device__ __forceinline__ void mma_commit_multicast(uint32_t bar, uint16_t cta_mask) {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-        " [%0], %1;" ::"r"(bar), "h"(cta_mask)
-        : "memory");
 }
 
 }  // namespace pk
@@ -414,24 +370,5 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity,
 }
 __device__ __forceinline__ void st_cluster_u32(uint32_t addr_cluster, uint32_t v) {
     asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr_cluster), "r"(v) : "memory");
-}
-}  // namespace pk
-
-namespace pk {
-// tma_prefetch_3d with an L2 eviction-priority policy for the prefetched lines.
-__device__ __forceinline__ void tma_prefetch_3d_hint(const CUtensorMap* map, int c0, int c1, int c2,
-                                                     uint64_t policy) {
-    asm volatile(
-        "cp.async.bulk.prefetch.tensor.3d.L2.global.tile.L2::cache_hint [%0, {%1, %2, %3}], %4;" ::"l"(
-            map),
-        "r"(c0), "r"(c1), "r"(c2), "l"(policy)
-        : "memory");
-}
-__device__ __forceinline__ void tma_prefetch_2d_hint(const CUtensorMap* map, int c0, int c1,
-                                                     uint64_t policy) {
-    asm volatile(
-        "cp.async.bulk.prefetch.tensor.2d.L2.global.tile.L2::cache_hint [%0, {%1, %2}], %3;" ::"l"(map),
-        "r"(c0), "r"(c1), "l"(policy)
-        : "memory");
 }
 }  // namespace pk
