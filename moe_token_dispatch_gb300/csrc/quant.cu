@@ -5,8 +5,10 @@
 // function of the bf16 inputs. When amax == 0 or 448 / amax overflows (amax
 // below about 1.3e-36), inv = scale = 1 and every code is zero. Inputs are
 // finite.
-//   k_quant_rows        activations x [T, D] -> codes [T, D] + scales [T]
-//                       (one warp per row, two passes over the row).
+//   k_quant_rows_reg    activations x [T, D] -> codes [T, D] + scales [T]
+//                       (one block per row held in registers, x read once;
+//                       D <= 8192), else
+//   k_quant_rows        the same with one warp per row and two passes.
 //   k_col_amax,
 //   k_col_convert,
 //   k_col_scale         weights W [E, D, N] -> codes in the blocked layout
@@ -76,6 +78,60 @@ __global__ void __launch_bounds__(256)
     }
 }
 
+// One block of kRowThreads per row, the row held in registers (VPT 16-byte
+// vectors per thread, D <= kRowThreads * 8 * VPT): x is read once; the
+// block's amax comes from warp shuffles and one shared-memory step.
+constexpr int kRowThreads = 256;
+template <int VPT>
+__global__ void __launch_bounds__(kRowThreads)
+    k_quant_rows_reg(const uint16_t* __restrict__ x, int32_t T, int32_t D,
+                     uint8_t* __restrict__ q, float* __restrict__ scale) {
+    __shared__ float wmax[kRowThreads / 32];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    for (int64_t t = blockIdx.x; t < T; t += gridDim.x) {
+        const uint16_t* row = x + t * D;
+        uint4 v[VPT];
+        float amax = 0.0f;
+#pragma unroll
+        for (int i = 0; i < VPT; ++i) {
+            const int c = (i * kRowThreads + threadIdx.x) * 8;
+            v[i] = c < D ? *reinterpret_cast<const uint4*>(row + c) : make_uint4(0, 0, 0, 0);
+            const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+#pragma unroll
+            for (int h = 0; h < 4; ++h)
+                amax = fmaxf(amax, fmaxf(fabsf(bf16_bits_to_f32(w[h] & 0xffffu)),
+                                         fabsf(bf16_bits_to_f32(w[h] >> 16))));
+        }
+        for (int d = 16; d > 0; d >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, d));
+        if (lane == 0) wmax[warp] = amax;
+        __syncthreads();
+        amax = wmax[0];
+#pragma unroll
+        for (int w = 1; w < kRowThreads / 32; ++w) amax = fmaxf(amax, wmax[w]);
+        __syncthreads();  // wmax is rewritten by the next row
+        const float inv = inv_scale(amax);
+        if (threadIdx.x == 0) scale[t] = scale_of(amax);
+        uint8_t* qrow = q + t * D;
+#pragma unroll
+        for (int i = 0; i < VPT; ++i) {
+            const int c = (i * kRowThreads + threadIdx.x) * 8;
+            if (c < D) {
+                const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+                uint32_t o[2];
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const uint16_t a = e4m3x2(__fmul_rn(bf16_bits_to_f32(w[2 * h] & 0xffffu), inv),
+                                              __fmul_rn(bf16_bits_to_f32(w[2 * h] >> 16), inv));
+                    const uint16_t b = e4m3x2(__fmul_rn(bf16_bits_to_f32(w[2 * h + 1] & 0xffffu), inv),
+                                              __fmul_rn(bf16_bits_to_f32(w[2 * h + 1] >> 16), inv));
+                    o[h] = static_cast<uint32_t>(a) | (static_cast<uint32_t>(b) << 16);
+                }
+                *reinterpret_cast<uint2*>(qrow + c) = make_uint2(o[0], o[1]);
+            }
+        }
+    }
+}
+
 // amax of every column of W[e] into amax_out[e, n]
 __global__ void __launch_bounds__(256)
     k_col_amax(const uint16_t* __restrict__ W, int32_t D, int32_t N, float* __restrict__ amax_out) {
@@ -140,6 +196,14 @@ cudaError_t launch_quant_rows(const uint16_t* x, int32_t T, int32_t D, uint8_t* 
     if (err != cudaSuccess) return err;
     err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (err != cudaSuccess) return err;
+    if (D <= kRowThreads * 8 * 4) {  // the row fits the block's registers: one read of x
+        const int grid = static_cast<int>(T < sms * 64 ? T : sms * 64);
+        if (D <= kRowThreads * 8 * 2)
+            k_quant_rows_reg<2><<<grid, kRowThreads, 0, stream>>>(x, T, D, q, scale);
+        else
+            k_quant_rows_reg<4><<<grid, kRowThreads, 0, stream>>>(x, T, D, q, scale);
+        return cudaGetLastError();
+    }
     const int64_t blocks = (static_cast<int64_t>(T) + 7) / 8;
     const int grid = static_cast<int>(blocks < sms * 16 ? blocks : sms * 16);
     k_quant_rows<<<grid, 256, 0, stream>>>(x, T, D, q, scale);

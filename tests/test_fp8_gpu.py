@@ -63,9 +63,10 @@ def _awkward_bf16(rng, shape):
     return bits
 
 
-def test_quant_rows_bit_exact(gpu_lib):
+@pytest.mark.parametrize("D", [7168 + 8, 8192 + 8, 64])  # block-per-row kernel, two-pass kernel, tiny
+def test_quant_rows_bit_exact(gpu_lib, D):
     rng = np.random.default_rng(3)
-    T, D = 301, 7168 + 8
+    T = 301
     x = ig.normal_bf16(1, ig.STREAM_X, 0, T * D).reshape(T, D)
     x[5] = 0                     # all-zero row: scale 1, codes 0
     x[6] = _awkward_bf16(rng, (D,))
