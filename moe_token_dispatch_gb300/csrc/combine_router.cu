@@ -21,6 +21,15 @@
 namespace pk {
 
 // ------------------------------------------------------------------ router
+// Unsigned key with the order of the float values (finite or infinite, not
+// NaN): negative floats have their bits inverted, the rest their sign bit set;
+// -0 is mapped like +0, so keys of equal values are equal. Non-negative keys
+// start at 0x80000000, so 0 is below every real value.
+__device__ __forceinline__ uint32_t order_key(float f) {
+    const uint32_t u = __float_as_uint(f == 0.0f ? 0.0f : f);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
 // PER = logits held per lane (E <= 32 * PER), a power of two so that the
 // selection loops are fully unrolled for the common expert counts.
 template <int PER>
@@ -54,18 +63,18 @@ __global__ void __launch_bounds__(256)
                     bv = v[i];
                     bi = i * 32 + lane;
                 }
-            for (int d = 16; d > 0; d >>= 1) {
-                const float ov = __shfl_xor_sync(0xffffffffu, bv, d);
-                const int oi = __shfl_xor_sync(0xffffffffu, bi, d);
-                if (oi != kNone && (bi == kNone || ov > bv || (ov == bv && oi < bi))) {
-                    bv = ov;
-                    bi = oi;
-                }
-            }
-            if ((bi & 31) == lane) avail &= ~(1u << (bi >> 5));
+            // warp arg-max in two reductions: the largest value (as an
+            // order-preserving integer key, -0 folded into +0 so that equal
+            // logits compare equal), then the lowest index holding it
+            const uint32_t key = bi == kNone ? 0u : order_key(bv);
+            const uint32_t kmax = __reduce_max_sync(0xffffffffu, key);
+            const int wi = static_cast<int>(__reduce_min_sync(
+                0xffffffffu, key == kmax && bi != kNone ? static_cast<uint32_t>(bi) : 0xffffffffu));
+            const float wv = __shfl_sync(0xffffffffu, bv, wi & 31);
+            if ((wi & 31) == lane) avail &= ~(1u << (wi >> 5));
             if (lane == s) {
-                my_val = bv;
-                my_idx = bi;
+                my_val = wv;
+                my_idx = wi;
             }
         }
         // softmax over the selected logits, shifted by the largest (slot 0)

@@ -49,6 +49,11 @@ def test_router_ties_and_infinities(gpu_lib):
     l = rng.integers(-2, 3, size=(200, 64)).astype(np.float32)   # many equal logits
     l[::7, ::3] = -np.inf
     _check_router(gpu_lib, l, 8)
+    # signed zeros compare equal: -0 and +0 logits tie and go to the lower expert
+    z = np.zeros((50, 40), dtype=np.float32)
+    z[rng.random(z.shape) < 0.5] = -0.0
+    z[::5, 7] = 1.0
+    _check_router(gpu_lib, z, 5)
 
 
 def _combine_gpu(pk, src, inv, gates, T, k):
