@@ -151,42 +151,56 @@ struct Unit {
     bool shared_w;  // other units of this expert load the same W tiles
 };
 
-// Walks the unit numbering; u must not decrease between calls.
+// Walks the unit numbering; u must not decrease between calls. Each expert
+// costs one load of its end offset; advance_once() takes at most one step, so
+// the roles can spread the walk to their next unit over the K-steps of the
+// current one instead of paying for it (a dozen experts at ep) at the unit
+// boundary.
 struct Walker {
     const int32_t* off;
     int E, R, De;
+    int nt256, nt128;  // n-tiles of 256 and of 128 columns
     int e;
     int64_t base;  // units of experts < e
+    int a_cur;     // clamp(off[e], 0, R)
+    int a_nxt;     // clamp(off[e + 1], 0, R)
     int lo, rows, groups, mpu_max, bn_max, ntiles;
     int64_t units;
 
     __device__ void init(const int32_t* o, int E_, int R_, int De_) {
         off = o; E = E_; R = R_; De = De_;
+        nt256 = (De + 255) >> 8;
+        nt128 = (De + 127) >> 7;
         e = 0; base = 0;
+        a_cur = min(max(__ldg(off), 0), R);
         load();
     }
+    // expert e's segment [a, b): a = clamp(off[e], 0, R), b = clamp(off[e+1], a, R)
     __device__ void load() {
         if (e >= E) { units = 0; return; }
-        int a = __ldg(off + e), b = __ldg(off + e + 1);
-        a = min(max(a, 0), R);
-        b = min(max(b, a), R);
-        lo = a;
-        rows = b - a;
+        a_nxt = min(max(__ldg(off + e + 1), 0), R);
+        lo = a_cur;
+        rows = max(a_nxt, a_cur) - a_cur;
         const int mt = (rows + BM - 1) / BM;
         if (mt == 3) {
-            mpu_max = 3; bn_max = 128;
+            mpu_max = 3; bn_max = 128; groups = 1; ntiles = nt128;
         } else {
-            mpu_max = 2; bn_max = 256;
+            mpu_max = 2; bn_max = 256; groups = (mt + 1) >> 1; ntiles = nt256;
         }
-        groups = (mt + mpu_max - 1) / mpu_max;
-        ntiles = (De + bn_max - 1) / bn_max;
         units = static_cast<int64_t>(groups) * ntiles;
     }
-    __device__ bool find(int64_t u, Unit& U) {
-        while (e < E && u >= base + units) {
+    __device__ __forceinline__ bool advance_once(int64_t u) {
+        if (e < E && u >= base + units) {
             base += units;
             ++e;
+            a_cur = a_nxt;
             load();
+            return true;
+        }
+        return false;
+    }
+    __device__ bool find(int64_t u, Unit& U) {
+        while (advance_once(u)) {
         }
         if (e >= E) return false;
         const int l = static_cast<int>(u - base);
@@ -394,6 +408,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 cp_async_arrive_noinc(wfull0 + 8 * wc.s);
                 ac.next();
                 wc.next();
+                wk.advance_once(u + gridDim.x);  // toward the next unit
             }
         }
         // Copies still in flight must land before the CTA may exit.
@@ -453,6 +468,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                     }
                     wc.next();
                     ac.next();
+                    wk.advance_once(u + gridDim.x);  // toward the next unit
                 }
             }
             // Every copy this thread started must land before the CTA may exit.
@@ -523,6 +539,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                     mma_commit(aempty0 + 8 * ac.s);
                     wc.next();
                     ac.next();
+                    wk.advance_once(u + gridDim.x);  // toward the next unit, behind the MMAs
                 }
                 if (!ok) break;
                 mma_commit(acc_full);
