@@ -496,6 +496,25 @@ def run_op(args, wl):
         flops = 2.0 * R * wl.D * wl.De
         metric = (f"FP8 (E4M3) dispatch + expert GEMM TFLOP/s at T={wl.T} D={wl.D} E={wl.E} "
                   f"k={wl.k} D_expert={wl.De}")
+    elif args.op == "fp8_grouped_gemm":
+        # FP8 down-projection: h quantised per row, W2 per (expert, column), once
+        K, N = wl.De, wl.D
+        A = dev_bf16(ig.normal_bf16(wl.seed, 7, 0, R * K).reshape(R, K))
+        W2 = dev_bf16(ig.make_W(ig.custom(T=wl.T, D=K, E=wl.E, k=wl.k, De=N, seed=wl.seed)))
+        wq = torch.empty((pk.pk_moe_fp8_weight_bytes(wl.E, K, N),), dtype=torch.uint8, device=dev)
+        sw = torch.empty((wl.E, N), dtype=torch.float32, device=dev)
+        pk.pk_moe_quant_weights(W2, wq, sw, stream)
+        del W2
+        aq = torch.empty((R, K), dtype=torch.uint8, device=dev)
+        sa = torch.empty((R,), dtype=torch.float32, device=dev)
+        pk.pk_moe_quant_rows(A, aq, sa, stream)
+        out = torch.empty((R, N), dtype=torch.bfloat16, device=dev)
+        fn = lambda: pk.pk_moe_grouped_gemm_fp8(aq, sa, md.offsets, wq, sw, out, md.status, stream)
+        qfn = lambda: pk.pk_moe_quant_rows(A, aq, sa, stream)
+        touched = int((counts > 0).sum())
+        alg_bytes = R * K + touched * K * N + R * N * 2 + R * 4 + touched * N * 4 + (wl.E + 1) * 4
+        flops = 2.0 * R * K * N
+        metric = f"FP8 (E4M3) down-projection grouped GEMM TFLOP/s at R={R} K={K} N={N} E={wl.E}"
     else:
         raise SystemExit(f"unknown --op {args.op}")
     for _ in range(max(3, args.warmup)):
@@ -528,10 +547,11 @@ def run_op(args, wl):
         tf = flops / (med * 1e-3) / 1e12
         line["value"], line["unit"] = tf, "TFLOP/s"
         # FP8 peak: the measured bf16 peak times the nominal fp8/bf16 ratio (4.5 / 2.25)
-        tpeak = peaks["bf16_tflops"] * (2.0 if args.op == "fp8_gemm" else 1.0)
+        fp8_op = args.op in ("fp8_gemm", "fp8_grouped_gemm")
+        tpeak = peaks["bf16_tflops"] * (2.0 if fp8_op else 1.0)
         line["roofline"]["tensor"] = {"achieved": tf, "peak": tpeak, "unit": "TFLOP/s",
                                       "frac": tf / tpeak}
-        if args.op == "fp8_gemm":
+        if fp8_op:
             line["roofline"]["tensor"]["peak_kind"] = "measured bf16 x 2 (nominal fp8/bf16)"
             qa, qb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             qa.record(stream)
@@ -557,7 +577,8 @@ def main(argv=None):
                     help="dispatch GEMM kernel: auto (= single), single (one CTA per SM) or pair "
                          "(2-CTA clusters)")
     ap.add_argument("--op", default="dispatch_gemm",
-                    choices=["dispatch_gemm", "router", "combine", "grouped_gemm", "fp8_gemm"],
+                    choices=["dispatch_gemm", "router", "combine", "grouped_gemm", "fp8_gemm",
+                             "fp8_grouped_gemm"],
                     help="dispatch_gemm: the benchmark step; the others time one kernel")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)

@@ -205,6 +205,21 @@ int pk_moe_grouped_gemm(const uint16_t* A, const int32_t* expert_offsets, const 
                         int32_t* status_word, void* stream);
 
 /*
+ * FP8 variant of the grouped GEMM (E4M3 codes, as pk_moe_dispatch_gemm_fp8):
+ *   out[j, n] = bf16_rne( (sum_c E4M3(Aq[j, c]) * E4M3(wq[e, n, c])) * sa[j] * sw[e, n] )
+ * for every expert e and row j in [expert_offsets[e], expert_offsets[e+1]).
+ *   Aq   device uint8 codes [R, K] (pk_moe_quant_rows of A), 16-byte aligned
+ *   sa   device fp32 [R]
+ *   wq   device uint8, blocked codes of W2 [E, K, N] from pk_moe_quant_weights, 16-byte aligned
+ *   sw   device fp32 [E, N], 16-byte aligned
+ *   out  device bf16 [R, N], 16-byte aligned; rows of each segment written
+ * Requires K a multiple of 16, N a multiple of 8. Offsets are clamped into [0, R].
+ */
+int pk_moe_grouped_gemm_fp8(const uint8_t* Aq, const float* sa, const int32_t* expert_offsets,
+                            const uint8_t* wq, const float* sw, int32_t R, int32_t K, int32_t N,
+                            int32_t E, uint16_t* out, int32_t* status_word, void* stream);
+
+/*
  * Router top-k (the selection the expert-parallel workload of "Key claims",
  * Fig. 17 describes with top_k=8 of num_experts=256; the pages leave the
  * router itself open): for every token t,

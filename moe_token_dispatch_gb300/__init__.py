@@ -31,6 +31,7 @@ from ._binding import (  # noqa: F401
     pk_moe_dispatch_gemm_fp8,
     pk_moe_fp8_weight_bytes,
     pk_moe_grouped_gemm,
+    pk_moe_grouped_gemm_fp8,
     pk_moe_quant_rows,
     pk_moe_quant_weights,
     pk_moe_route_counts,

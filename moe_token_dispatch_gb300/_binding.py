@@ -64,6 +64,8 @@ def _load():
     lib.pk_moe_fp8_weight_bytes.argtypes = [I32, I32, I32]
     lib.pk_moe_quant_weights.restype = ctypes.c_int
     lib.pk_moe_quant_weights.argtypes = [P, I32, I32, I32, P, P, P]
+    lib.pk_moe_grouped_gemm_fp8.restype = ctypes.c_int
+    lib.pk_moe_grouped_gemm_fp8.argtypes = [P, P, P, P, P, I32, I32, I32, I32, P, P, P]
     lib.pk_moe_router_topk.restype = ctypes.c_int
     lib.pk_moe_router_topk.argtypes = [P, I32, I32, I32, P, P, P]
     lib.pk_moe_combine.restype = ctypes.c_int
@@ -230,6 +232,22 @@ def pk_moe_quant_weights(W: torch.Tensor, wq: torch.Tensor, sw: torch.Tensor,
                                   _ptr(wq, torch.uint8, "wq", pk_moe_fp8_weight_bytes(E, D, N)),
                                   _ptr(sw, torch.float32, "sw", E * N), _stream(stream))
     _check(rc, "pk_moe_quant_weights")
+
+
+def pk_moe_grouped_gemm_fp8(Aq: torch.Tensor, sa: torch.Tensor, expert_offsets: torch.Tensor,
+                            wq: torch.Tensor, sw: torch.Tensor, out: torch.Tensor,
+                            status_word: torch.Tensor | None = None, stream=None) -> None:
+    """Aq: uint8 codes [R, K]; wq: blocked codes of W2 [E, K, N]; sw: fp32 [E, N]."""
+    R, K = Aq.shape
+    E, N = sw.shape
+    rc = lib.pk_moe_grouped_gemm_fp8(
+        _ptr(Aq, torch.uint8, "Aq"), _ptr(sa, torch.float32, "sa", R),
+        _ptr(expert_offsets, torch.int32, "expert_offsets", E + 1),
+        _ptr(wq, torch.uint8, "wq", pk_moe_fp8_weight_bytes(E, K, N)),
+        _ptr(sw, torch.float32, "sw", E * N), R, K, N, E,
+        _ptr(out, torch.bfloat16, "out", R * N),
+        _ptr(status_word, torch.int32, "status_word", 1), _stream(stream))
+    _check(rc, "pk_moe_grouped_gemm_fp8")
 
 
 def pk_moe_router_topk(logits: torch.Tensor, k: int, topk_idx: torch.Tensor,

@@ -162,6 +162,21 @@ int pk_moe_grouped_gemm(const uint16_t* A, const int32_t* expert_offsets, const 
                                    g_wait_limit_ns.load(std::memory_order_relaxed));
 }
 
+int pk_moe_grouped_gemm_fp8(const uint8_t* Aq, const float* sa, const int32_t* expert_offsets,
+                            const uint8_t* wq, const float* sw, int32_t R, int32_t K, int32_t N,
+                            int32_t E, uint16_t* out, int32_t* status_word, void* stream) {
+    if (R < 0 || K < 1 || N < 1 || E < 1) return PK_ERR_INVALID_ARG;
+    if ((K % 16) != 0 || (N % 8) != 0) return PK_ERR_INVALID_ARG;
+    if (R == 0) return PK_OK;
+    if (!Aq || !sa || !expert_offsets || !wq || !sw || !out) return PK_ERR_INVALID_ARG;
+    if (!aligned16(Aq) || !aligned16(wq) || !aligned16(sw) || !aligned16(out))
+        return PK_ERR_INVALID_ARG;
+    if (pk_moe_fp8_weight_bytes(E, K, N) >= (size_t{1} << 38)) return PK_ERR_UNSUPPORTED;
+    return pk::launch_grouped_gemm_fp8(Aq, sa, expert_offsets, wq, sw, R, K, N, E, out,
+                                       status_word, static_cast<cudaStream_t>(stream),
+                                       g_wait_limit_ns.load(std::memory_order_relaxed));
+}
+
 int pk_moe_router_topk(const float* logits, int32_t T, int32_t E, int32_t k, int32_t* topk_idx,
                        float* gates, void* stream) {
     if (T < 0 || E < 1 || k < 1 || k > E || k > 32) return PK_ERR_INVALID_ARG;

@@ -33,7 +33,8 @@
 // The same kernel, instantiated with kGather = false, is the grouped GEMM of
 // rows that are already in expert order (the down-projection that follows the
 // expert MLP: out2[j, :] = h[j, :] @ W2[e(j)]): the W producer then also
-// TMA-loads each m-tile of A as one 128-row box, and the gather warps idle.
+// TMA-loads each m-tile of A as one 128-row box, and the gather warps idle
+// (with kFp8 too: E4M3 codes of h with one scale per row).
 //
 // With kFp8, the same pipeline is the FP8 variant of the expert GEMM: x and W
 // arrive as E4M3 codes with one fp32 scale per token row and per (expert,
@@ -577,10 +578,14 @@ __global__ void __launch_bounds__(THREADS, 1)
                 const int r = rbase + lane;
                 const bool valid = r < U.rows;
                 uint16_t* orow = out + static_cast<int64_t>(U.row0 + r) * De;
-                float rs = 1.0f;  // FP8: this row's token scale
+                float rs = 1.0f;  // FP8: this row's scale (its token's, or its own row's)
                 if (kFp8 && valid) {
-                    const int f = __ldg(perm + U.row0 + r);
-                    rs = (f >= 0 && f < R) ? __ldg(sx + f / k) : 0.0f;
+                    if (kGather) {
+                        const int f = __ldg(perm + U.row0 + r);
+                        rs = (f >= 0 && f < R) ? __ldg(sx + f / k) : 0.0f;
+                    } else {
+                        rs = __ldg(sx + U.row0 + r);
+                    }
                 }
                 const float* sw_e = kFp8 ? sw + static_cast<int64_t>(U.e) * De : nullptr;
                 const uint32_t tbase = tmem + (static_cast<uint32_t>(q * 32) << 16) +
@@ -724,6 +729,9 @@ int launch_common(bool gather, bool fp8, const void* A, const float* sx, const i
                                      SMEM_BYTES) != cudaSuccess ||
                 cudaFuncSetAttribute(k_dispatch_gemm<true, true>,
                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     SMEM_BYTES) != cudaSuccess ||
+                cudaFuncSetAttribute(k_dispatch_gemm<false, true>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      SMEM_BYTES) != cudaSuccess)
                 return PK_ERR_CUDA;
             di.attr_set = true;
@@ -737,20 +745,26 @@ int launch_common(bool gather, bool fp8, const void* A, const float* sx, const i
     if (gather) {
         amap = wmap;  // unused
     } else {
-        // A [T, D] row-major, boxes of 64 columns x 128 rows, 128-byte swizzle
+        // A [T, D] row-major, boxes of 128 bytes (64 bf16 or 128 E4M3 codes) x 128
+        // rows, 128-byte swizzle
         cuuint64_t dims[2] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(T)};
-        cuuint64_t strides[1] = {static_cast<cuuint64_t>(D) * 2};
-        cuuint32_t box[2] = {BK, BM};
+        cuuint64_t strides[1] = {static_cast<cuuint64_t>(D) * (fp8 ? 1 : 2)};
+        cuuint32_t box[2] = {fp8 ? static_cast<cuuint32_t>(ROW_BYTES) : static_cast<cuuint32_t>(BK),
+                             static_cast<cuuint32_t>(BM)};
         cuuint32_t es[2] = {1, 1};
-        if (enc(&amap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(A), dims, strides,
+        if (enc(&amap, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                const_cast<void*>(A), dims, strides,
                 box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return PK_ERR_UNSUPPORTED;
     }
     const uint8_t* a8 = static_cast<const uint8_t*>(A);
-    if (fp8)
+    if (fp8 && gather)
         k_dispatch_gemm<true, true><<<sms, THREADS, SMEM_BYTES, stream>>>(
             wmap, amap, a8, sx, sw, perm, offsets, out, T, k, D, E, De, status, wait_limit_ns);
+    else if (fp8)
+        k_dispatch_gemm<false, true><<<sms, THREADS, SMEM_BYTES, stream>>>(
+            wmap, amap, a8, sx, sw, nullptr, offsets, out, T, k, D, E, De, status, wait_limit_ns);
     else if (gather)
         k_dispatch_gemm<true, false><<<sms, THREADS, SMEM_BYTES, stream>>>(
             wmap, amap, a8, nullptr, nullptr, perm, offsets, out, T, k, D, E, De, status,
@@ -786,6 +800,14 @@ int launch_grouped_gemm(const uint16_t* A, const int32_t* offsets, const uint16_
                         cudaStream_t stream, uint64_t wait_limit_ns) {
     return launch_common(false, false, A, nullptr, nullptr, offsets, W, nullptr, R, 1, K, E, N,
                          out, status, stream, wait_limit_ns);
+}
+
+int launch_grouped_gemm_fp8(const uint8_t* Aq, const float* sa, const int32_t* offsets,
+                            const uint8_t* wq, const float* sw, int32_t R, int32_t K, int32_t N,
+                            int32_t E, uint16_t* out, int32_t* status, cudaStream_t stream,
+                            uint64_t wait_limit_ns) {
+    return launch_common(false, true, Aq, sa, nullptr, offsets, wq, sw, R, 1, K, E, N, out, status,
+                         stream, wait_limit_ns);
 }
 
 // ------------------------------------------------- bounded-wait check kernel

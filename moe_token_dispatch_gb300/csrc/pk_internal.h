@@ -55,6 +55,13 @@ cudaError_t launch_quant_rows(const uint16_t* x, int32_t T, int32_t D, uint8_t* 
 cudaError_t launch_quant_cols(const uint16_t* W, int32_t E, int32_t D, int32_t N, uint8_t* q,
                               float* scale, cudaStream_t stream);
 
+// FP8 grouped GEMM: E4M3 codes Aq [R, K] (scales sa [R]) and blocked W codes
+// (scales sw [E, N]).
+int launch_grouped_gemm_fp8(const uint8_t* Aq, const float* sa, const int32_t* offsets,
+                            const uint8_t* wq, const float* sw, int32_t R, int32_t K, int32_t N,
+                            int32_t E, uint16_t* out, int32_t* status, cudaStream_t stream,
+                            uint64_t wait_limit_ns);
+
 // Grouped GEMM of expert-sorted rows (no gather).
 int launch_grouped_gemm(const uint16_t* A, const int32_t* offsets, const uint16_t* W, int32_t R,
                         int32_t K, int32_t N, int32_t E, uint16_t* out, int32_t* status,

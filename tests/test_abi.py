@@ -154,3 +154,12 @@ def test_route_kernel_launches(lib):
     assert L.pk_moe_route_kernel_launches(8192, 8, 256) == 3
     assert L.pk_moe_route_kernel_launches(0, 8, 256) == 1
     assert L.pk_moe_route_kernel_launches(-1, 8, 256) == -1
+
+
+def test_grouped_gemm_fp8_rejects(lib):
+    L = _raw(lib)
+    # Aq, sa, offsets, wq, sw, R, K, N, E, out, status, stream
+    assert L.pk_moe_grouped_gemm_fp8(FAKE, FAKE, FAKE, FAKE, FAKE, 8, 56, 64, 2, FAKE, None, None) == 1
+    assert L.pk_moe_grouped_gemm_fp8(FAKE, FAKE, FAKE, FAKE, FAKE, 8, 64, 12, 2, FAKE, None, None) == 1
+    assert L.pk_moe_grouped_gemm_fp8(FAKE, None, FAKE, FAKE, FAKE, 8, 64, 64, 2, FAKE, None, None) == 1
+    assert L.pk_moe_grouped_gemm_fp8(None, None, None, None, None, 0, 64, 64, 2, None, None, None) == 0

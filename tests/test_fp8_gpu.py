@@ -266,3 +266,29 @@ def test_fp8_full_size_sampled(gpu_lib, name):
     want = oracle.gemm_fp8_rows(xq, sx, ref["perm"], offsets, wq_full, sw_full, wl.k, rows)
     got = bf16_dev_to_f64(out[torch.from_numpy(rows).cuda()])
     assert_gemm_close(got, want, rows)
+
+
+@pytest.mark.parametrize("RT,K,E,k,N", [(512, 640, 4, 2, 576), (300, 208, 3, 1, 200),
+                                        (1000, 128, 2, 2, 256)])
+def test_fp8_grouped_gemm(gpu_lib, RT, K, E, k, N):
+    """Down-projection on E4M3 codes: rows already in expert order (A's row
+    j is its own token, so the oracle's perm is the identity with k = 1)."""
+    pk = gpu_lib
+    wl = ig.custom(T=RT, D=K, E=E, k=k, De=N, seed=14)
+    topk = ig.make_topk(wl)
+    _, offsets = oracle.route_counts(topk, E)
+    R = RT * k
+    A = ig.normal_bf16(14, 7, 0, R * K).reshape(R, K)
+    W2 = ig.make_W(wl)
+    aq, sa = oracle.quant_rows(A)
+    wq, sw = oracle.quant_cols(W2)
+    out = torch.full((R, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pk.pk_moe_grouped_gemm_fp8(_u8_dev(aq), torch.from_numpy(sa).cuda(),
+                               torch.from_numpy(offsets.astype(np.int32)).cuda(),
+                               _u8_dev(to_blocked(wq)), torch.from_numpy(sw).cuda(), out, st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    rows = np.arange(R, dtype=np.int64)
+    want = oracle.gemm_fp8_rows(aq, sa, rows, offsets, wq, sw, 1, rows)
+    assert_gemm_close(bf16_dev_to_f64(out), want, rows)
