@@ -535,7 +535,8 @@ def run_op(args, wl):
     # ncu summaries of the kernels beside the step (prefix, source file)
     op_profile = {"combine": ("combine", "combine_router.cu"),
                   "grouped_gemm": ("grouped_gemm", "dispatch_gemm.cu"),
-                  "fp8_gemm": ("fp8_dispatch_gemm", "dispatch_gemm.cu")}.get(args.op)
+                  "fp8_gemm": ("fp8_dispatch_gemm", "dispatch_gemm.cu"),
+                  "fp8_grouped_gemm": ("fp8_grouped_gemm", "dispatch_gemm.cu")}.get(args.op)
     traffic = (profiled_traffic(wl.name, prefix=op_profile[0], src=op_profile[1])
                if op_profile else None)
     line = {"op": args.op, "metric": metric, "workload": wl.name, "ms_median": med,
