@@ -68,3 +68,36 @@ def test_reference_arm_line(capsys):
     assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["value"] > 0
     assert line["steps"] == 2 and line["warmup"] == 3
+
+
+def test_profiled_traffic_follows_the_kernel_source(tmp_path, monkeypatch):
+    """traffic comes from profiles/<prefix>_<workload>.md (else its smaller
+    stand-in, scaled) only while the recorded source hash matches."""
+    prof = tmp_path / "profiles"
+    src_dir = tmp_path / "moe_token_dispatch_gb300" / "csrc"
+    prof.mkdir()
+    src_dir.mkdir(parents=True)
+    (src_dir / "k.cu").write_text("kernel v1\n")
+    digest = bench.source_digest(str(src_dir / "k.cu"))
+    (prof / "kk_ep32.md").write_text(f"kernel_source_sha256_16: {digest}\n"
+                                     "traffic_bytes_per_launch: 1.0e+09\n")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.profiled_traffic("ep", prefix="kk", src="k.cu") == 1.0e9 * 256 / 32
+    (prof / "kk_ep.md").write_text(f"kernel_source_sha256_16: {digest}\n"
+                                   "traffic_bytes_per_launch: 3.0e+09\n")
+    assert bench.profiled_traffic("ep", prefix="kk", src="k.cu") == 3.0e9   # direct capture wins
+    (src_dir / "k.cu").write_text("kernel v2\n")                             # source changed
+    assert bench.profiled_traffic("ep", prefix="kk", src="k.cu") is None
+
+
+def test_committed_profiles_carry_hash_and_traffic():
+    import re
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    pdir = os.path.join(root, "profiles")
+    for name in os.listdir(pdir):
+        if name == "launches_ep.md":
+            continue
+        text = open(os.path.join(pdir, name)).read()
+        assert re.search(r"kernel_source_sha256_16: [0-9a-f]{16}", text), name
+        assert re.search(r"traffic_bytes_per_launch: [0-9.eE+]+", text), name
+        assert "ncu " in text and "--clock-control none" in text, name
