@@ -59,7 +59,10 @@ typedef enum {
 /* Static string naming a status code (never NULL). */
 const char* pk_status_str(int status);
 
-/* Version of this ABI (major * 10000 + minor * 100 + patch). */
+/* Version of this ABI (major * 10000 + minor * 100 + patch). 1.1: FP8
+ * entry points (quantisation, dispatch and grouped GEMM), GEMM kernel
+ * selection, routing launch count. */
+#define PK_ABI_VERSION 10100
 int pk_abi_version(void);
 
 /*

@@ -38,7 +38,7 @@ const char* pk_status_str(int status) {
     }
 }
 
-int pk_abi_version(void) { return 10000; }
+int pk_abi_version(void) { return PK_ABI_VERSION; }
 
 size_t pk_moe_workspace_bytes(int32_t T, int32_t k, int32_t E) {
     if (T <= 0 || k <= 0 || E <= 0) return 0;

@@ -43,6 +43,9 @@ def test_status_strings(lib):
     assert lib.pk_status_str(lib.PK_ERR_TIMEOUT) == "PK_ERR_TIMEOUT"
     assert lib.pk_status_str(99) == "PK_ERR_UNKNOWN"
     assert lib.pk_abi_version() >= 10000
+    import re
+    m = re.search(r"#define PK_ABI_VERSION (\d+)", open(HEADER).read())
+    assert m and lib.pk_abi_version() == int(m.group(1))
 
 
 def test_workspace_bytes(lib):
