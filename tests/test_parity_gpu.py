@@ -79,7 +79,9 @@ def test_skewed_routing_small(gpu_lib, gemm_kernel):
 
 
 @pytest.mark.parametrize("T,k,E", [
-    (2048, 8, 4096),    # 8 chunks x 4096 experts: three kernels (histogram, scan, permutation)
+    (2048, 8, 4096),    # 8 chunks x 4096 experts: three kernels, chunk rows scanned in place
+    (16384, 8, 256),    # 64 chunks: chunk rows staged in 67 KiB of shared memory by the scan
+    (32768, 8, 256),    # 128 chunks: 128 KiB of chunk rows, scanned in place
     (512, 8, 4096),     # two chunks x 4096 experts: one-block counts + scan, 64 KiB of shared memory
     (100, 3, 7),        # one ragged chunk
 ])
