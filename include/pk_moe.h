@@ -23,7 +23,12 @@
  * Calls are asynchronous on `stream` (a cudaStream_t passed as void*; NULL is
  * the legacy default stream) and do not synchronise. route_counts ->
  * build_perm -> dispatch_gemm must be ordered on one stream (or by events).
- * Calls on distinct streams with distinct buffers are thread safe.
+ * Calls on distinct streams with distinct buffers are thread safe. The
+ * routing kernels are launched with programmatic stream serialisation: one
+ * may be scheduled while the kernel ahead of it in the stream is finishing,
+ * but it waits for that kernel to complete before its first read or write of
+ * global memory, so stream order holds for every buffer (also under CUDA
+ * graph capture).
  *
  * Return value: PK_OK, or the first synchronous failure -- argument checks
  * (PK_ERR_INVALID_ARG, PK_ERR_UNSUPPORTED) or a failed launch (PK_ERR_CUDA).
