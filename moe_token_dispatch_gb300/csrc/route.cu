@@ -16,7 +16,9 @@
 //                  of two; on larger arrays one SM's __match_any_sync rate
 //                  makes it slower than the spread-out histogram);
 //   k_build_perm   each warp of block b owns a contiguous run of the chunk
-//                  (8 entries per lane, loaded once into registers); a
+//                  (2 entries per lane in 32-warp blocks when 32 warp
+//                  histograms of E counters fit 48 KiB, else 8 per lane in
+//                  8-warp blocks; loaded once into registers); a
 //                  per-warp histogram and a scan over warps give every warp
 //                  its first position per expert, then warps walk their runs
 //                  32 entries at a time and rank equal experts inside a warp
@@ -250,15 +252,17 @@ __global__ void __launch_bounds__(kScanThreads)
     if (threadIdx.x == 0) offsets[E] = total;
 }
 
-__global__ void __launch_bounds__(kRouteThreads)
+template <int kWarps>
+__global__ void __launch_bounds__(kWarps * 32)
     k_build_perm(const int32_t* __restrict__ topk, int32_t R, int32_t E,
                  const int32_t* __restrict__ blockbase, int32_t* __restrict__ perm,
                  int32_t* __restrict__ inv_perm, int32_t* status) {
-    extern __shared__ int32_t wpos[];  // [kRouteWarps][E]
-    constexpr int kPerWarp = kRouteChunk / kRouteWarps;
+    extern __shared__ int32_t wpos[];  // [kWarps][E]
+    static_assert(kRouteChunk % (kWarps * 32) == 0, "whole 32-entry rounds per warp");
+    constexpr int kPerWarp = kRouteChunk / kWarps;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const uint32_t lt_mask = (1u << lane) - 1u;
-    for (int i = threadIdx.x; i < kRouteWarps * E; i += blockDim.x) wpos[i] = 0;
+    for (int i = threadIdx.x; i < kWarps * E; i += blockDim.x) wpos[i] = 0;
     grid_dep_wait();
     grid_dep_release();
     // This block's starting position of expert threadIdx.x, fetched now so
@@ -299,7 +303,7 @@ __global__ void __launch_bounds__(kRouteThreads)
     // Pass 2: first position of every warp's entries, per expert.
     for (int e = threadIdx.x; e < E; e += blockDim.x) {
         int32_t r = e == static_cast<int>(threadIdx.x) ? bb_first : bb[e];
-        for (int w = 0; w < kRouteWarps; ++w) {
+        for (int w = 0; w < kWarps; ++w) {
             const int32_t c = wpos[w * E + e];
             wpos[w * E + e] = r;
             r += c;
@@ -329,6 +333,9 @@ __global__ void __launch_bounds__(kRouteThreads)
     }
     if (bad) report(status, PK_ERR_BAD_INDEX);
 }
+
+// Warps of the permutation kernel's wide form (1024 threads).
+constexpr int kPermWideWarps = 32;
 
 namespace {
 int g_perm_smem_set[64] = {0};
@@ -411,14 +418,20 @@ cudaError_t launch_build_perm(const int32_t* topk, int32_t R, int32_t E,
                               int32_t* status, cudaStream_t stream) {
     const int nblk = route_blocks(R);
     if (nblk == 0) return cudaSuccess;
+    // 32 warps (2 entries per lane: four rounds of __match_any_sync ranking
+    // instead of sixteen) when their histograms fit the default 48 KiB.
+    const size_t smem32 = sizeof(int32_t) * kPermWideWarps * static_cast<size_t>(E);
+    if (smem32 <= 48 * 1024)
+        return launch_chained(k_build_perm<kPermWideWarps>, nblk, kPermWideWarps * 32, smem32,
+                              stream, topk, R, E, blockbase, perm, inv_perm, status);
     const size_t smem = sizeof(int32_t) * kRouteWarps * static_cast<size_t>(E);
     if (smem > 48 * 1024) {
-        const cudaError_t err = allow_smem(k_build_perm, g_perm_smem_set,
+        const cudaError_t err = allow_smem(k_build_perm<kRouteWarps>, g_perm_smem_set,
                                            sizeof(int32_t) * kRouteWarps * PK_MAX_EXPERTS);
         if (err != cudaSuccess) return err;
     }
-    return launch_chained(k_build_perm, nblk, kRouteThreads, smem, stream, topk, R, E, blockbase,
-                          perm, inv_perm, status);
+    return launch_chained(k_build_perm<kRouteWarps>, nblk, kRouteThreads, smem, stream, topk, R, E,
+                          blockbase, perm, inv_perm, status);
 }
 
 }  // namespace pk
