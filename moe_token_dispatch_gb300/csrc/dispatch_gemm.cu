@@ -42,7 +42,9 @@
 // W is read K-major from a blocked layout in which each 64-column x 128-code
 // box is one contiguous 8 KiB block (so every TMA box is a single contiguous
 // read from HBM), the MMAs are tcgen05.mma kind::f8f6f4 with K = 32, and the
-// epilogue multiplies each accumulator by its row's and column's scale.
+// epilogue multiplies each accumulator by its row's and column's scale (both
+// loaded into registers while the unit's MMAs still run, so that the
+// accumulators are not held in TMEM across those loads).
 //
 // Work unit = (expert e, group of m-tiles, n-tile), with a shape chosen per
 // expert so that TMEM (512 fp32 columns x 128 lanes) holds every accumulator
@@ -561,6 +563,30 @@ __global__ void __launch_bounds__(THREADS, 1)
         for (int64_t u = blockIdx.x;; u += gridDim.x) {
             Unit U;
             if (!wk.find(u, U)) break;
+            // FP8: this lane's row scales (one per m-tile) and column scales
+            // (one per 32 columns), loaded while the unit's MMAs still run.
+            float rs_pre[MAX_MPU] = {1.0f, 1.0f, 1.0f};
+            float cs_pre[8] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
+            if (kFp8) {
+#pragma unroll
+                for (int mt = 0; mt < MAX_MPU; ++mt) {
+                    const int r = mt * BM + q * 32 + lane;
+                    if (mt < U.mpu && r < U.rows) {
+                        if (kGather) {
+                            const int f = __ldg(perm + U.row0 + r);
+                            rs_pre[mt] = (f >= 0 && f < R) ? __ldg(sx + f / k) : 0.0f;
+                        } else {
+                            rs_pre[mt] = __ldg(sx + U.row0 + r);
+                        }
+                    }
+                }
+                const float* sw_u = sw + static_cast<int64_t>(U.e) * De;
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    const int col = U.n0 + c * 32 + lane;
+                    if (c * 32 < U.bn && col < De) cs_pre[c] = __ldg(sw_u + col);
+                }
+            }
             if (!warp_wait(acc_full, acc_phase, abort, limit)) {
                 if (lane == 0) fail(abort, status);
                 break;
@@ -578,26 +604,20 @@ __global__ void __launch_bounds__(THREADS, 1)
                 const int r = rbase + lane;
                 const bool valid = r < U.rows;
                 uint16_t* orow = out + static_cast<int64_t>(U.row0 + r) * De;
-                float rs = 1.0f;  // FP8: this row's scale (its token's, or its own row's)
-                if (kFp8 && valid) {
-                    if (kGather) {
-                        const int f = __ldg(perm + U.row0 + r);
-                        rs = (f >= 0 && f < R) ? __ldg(sx + f / k) : 0.0f;
-                    } else {
-                        rs = __ldg(sx + U.row0 + r);
-                    }
-                }
-                const float* sw_e = kFp8 ? sw + static_cast<int64_t>(U.e) * De : nullptr;
+                // FP8: this row's scale (its token's, or its own row's)
+                const float rs = mt == 0 ? rs_pre[0] : (mt == 1 ? rs_pre[1] : rs_pre[2]);
                 const uint32_t tbase = tmem + (static_cast<uint32_t>(q * 32) << 16) +
                                        static_cast<uint32_t>(mt * U.bn_max);
                 for (int cc = 0; cc < U.bn / 32; cc += 2) {
-                    // FP8: this lane's column scales, loaded before the TMEM reads
-                    float cs0 = 0.0f, cs1 = 0.0f;
-                    if (kFp8) {
-                        const int ca = U.n0 + cc * 32 + lane, cb = ca + 32;
-                        if (ca < De) cs0 = __ldg(sw_e + ca);
-                        if (cb < De) cs1 = __ldg(sw_e + cb);
-                    }
+                    // FP8: this lane's column scales (loaded before the accumulators were ready)
+                    const float cs0 = cc == 0   ? cs_pre[0]
+                                      : cc == 2 ? cs_pre[2]
+                                      : cc == 4 ? cs_pre[4]
+                                                : cs_pre[6];
+                    const float cs1 = cc == 0   ? cs_pre[1]
+                                      : cc == 2 ? cs_pre[3]
+                                      : cc == 4 ? cs_pre[5]
+                                                : cs_pre[7];
                     uint32_t v0[32], v1[32];
                     tmem_ld_32x32b_x32(tbase + cc * 32, v0);
                     tmem_ld_32x32b_x32(tbase + cc * 32 + 32, v1);
