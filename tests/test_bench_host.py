@@ -57,6 +57,7 @@ def test_workload_bytes_counts_only_touched_experts():
     assert b["experts_touched"] == 2
     assert b["w_touched"] == 2 * 16 * 8 * 2
     assert b["x_gathered"] == 8 * 16 * 2 and b["out"] == 8 * 8 * 2
+    assert b["x_unique"] == 4 * 16 * 2   # each token row once: a lower bound, not in the sum
 
 
 def test_reference_arm_line(capsys):
