@@ -19,16 +19,24 @@
 //   warps 6,7,9,10  dispatch: gather the unit's routed x rows with 16-byte
 //              cp.async into K-major 128-byte-swizzled tiles (each warp
 //              instruction moves four whole 128-byte row segments); each
-//              thread's copies arrive on the slots' barriers when they land,
-//              and the MMA thread fences them into the async proxy after its
-//              wait, before the tensor cores read them.
-// Warp 8 only waits at the final barrier: warps share an SM sub-partition
-// with the warps whose index is equal mod 4, and this keeps the busy gather
-// warps off the MMA issuer's sub-partition.
-// Two rings of shared-memory slots (full/empty mbarriers) connect producers
-// and MMA: four 32 KiB W slots and three 32 KiB A slots, one of each per
-// K-step. W comes from HBM and takes longest to arrive, so it runs up to four
-// K-steps ahead; the gathered rows mostly hit L2 and run three ahead.
+//              thread's copies arrive on the K-step's full barrier when they
+//              land, and the MMA thread fences them into the async proxy after
+//              its wait, before the tensor cores read them.
+//   warp 8     scheduler: walks this CTA's units 32 experts at a time (one
+//              expert per lane) and queues each unit's shape in shared memory
+//              (eight entries, full/empty barriers), so no other role walks
+//              the expert offsets. Warps share an SM sub-partition with the
+//              warps whose index is equal mod 4; this keeps the busy gather
+//              warps off the MMA issuer's sub-partition.
+// Two rings of shared-memory slots connect producers and MMA: four 32 KiB W
+// slots and three 32 KiB A slots, one of each per K-step. W comes from HBM
+// and takes longest to arrive, so it runs up to four K-steps ahead; the
+// gathered rows mostly hit L2 and run three ahead. One full and one empty
+// barrier per K-step (indexed by the W slot) serve both rings: the full
+// barrier counts the W bytes and every gather thread's arrival, so the MMA
+// thread waits once per K-step, and its one commit frees both slots (a
+// producer of the A ring waits for the K-step three back, which also frees
+// the W slot four back).
 //
 // The same kernel, instantiated with kGather = false, is the grouped GEMM of
 // rows that are already in expert order (the down-projection that follows the
@@ -115,14 +123,20 @@ __device__ __forceinline__ int gather_index(int warp, int lane) {
 constexpr int ROWS_PER_PASS = GATHER_THREADS / 8;    // 8 threads per 128-byte row segment
 constexpr int ROWS_PER_THREAD = BM / ROWS_PER_PASS;  // per m-tile
 constexpr int MAX_MPU = 3;                   // m-tiles per unit
+constexpr int SCHED_WARP = 8;
+constexpr int NQ = 8;                        // unit queue depth
+constexpr int QWORDS = 8;                    // e, row0, rows, mpu, n0, bn, bn_max, shared_w
 struct Ctrl {
+    // One pair of barriers per K-step covers both rings: the K-step's W slot
+    // and A slot fill up together and are freed by the same commit.
     uint64_t wfull[W_STAGES];   // W producer arrive + tx bytes (+ one arrival per gather thread)
     uint64_t wempty[W_STAGES];  // one tcgen05.commit
-    uint64_t afull[A_STAGES];   // one arrival per gather thread (grouped GEMM: W producer + tx)
-    uint64_t aempty[A_STAGES];  // one tcgen05.commit
     uint64_t acc_full;          // one tcgen05.commit per unit
     uint64_t acc_empty;         // one arrive per epilogue warp
     uint64_t drain;
+    uint64_t qfull[NQ];         // scheduler arrive
+    uint64_t qempty[NQ];        // one arrive per consumer (thread or warp)
+    int q[NQ][QWORDS];
     uint32_t tmem_base;
     int abort;
 };
@@ -143,6 +157,17 @@ struct Cursor {
     }
 };
 
+// Cursor over the W ring that trails the current K-step by A_STAGES: slot
+// (j - A_STAGES) mod W_STAGES and the parity of that K-step's phase. Its
+// first A_STAGES positions name phase -1 (parity 1), which a fresh barrier
+// reports complete, so the first fills of the A ring do not wait.
+__device__ __forceinline__ Cursor<W_STAGES> lag_cursor() {
+    Cursor<W_STAGES> c;
+    c.s = (W_STAGES - A_STAGES) % W_STAGES;
+    c.ph = 1u;
+    return c;
+}
+
 struct Unit {
     int e;        // expert
     int row0;     // first sorted row of the unit
@@ -154,72 +179,6 @@ struct Unit {
     bool shared_w;  // other units of this expert load the same W tiles
 };
 
-// Walks the unit numbering; u must not decrease between calls. Each expert
-// costs one load of its end offset; advance_once() takes at most one step, so
-// the roles can spread the walk to their next unit over the K-steps of the
-// current one instead of paying for it (a dozen experts at ep) at the unit
-// boundary.
-struct Walker {
-    const int32_t* off;
-    int E, R, De;
-    int nt256, nt128;  // n-tiles of 256 and of 128 columns
-    int e;
-    int64_t base;  // units of experts < e
-    int a_cur;     // clamp(off[e], 0, R)
-    int a_nxt;     // clamp(off[e + 1], 0, R)
-    int lo, rows, groups, mpu_max, bn_max, ntiles;
-    int64_t units;
-
-    __device__ void init(const int32_t* o, int E_, int R_, int De_) {
-        off = o; E = E_; R = R_; De = De_;
-        nt256 = (De + 255) >> 8;
-        nt128 = (De + 127) >> 7;
-        e = 0; base = 0;
-        a_cur = min(max(__ldg(off), 0), R);
-        load();
-    }
-    // expert e's segment [a, b): a = clamp(off[e], 0, R), b = clamp(off[e+1], a, R)
-    __device__ void load() {
-        if (e >= E) { units = 0; return; }
-        a_nxt = min(max(__ldg(off + e + 1), 0), R);
-        lo = a_cur;
-        rows = max(a_nxt, a_cur) - a_cur;
-        const int mt = (rows + BM - 1) / BM;
-        if (mt == 3) {
-            mpu_max = 3; bn_max = 128; groups = 1; ntiles = nt128;
-        } else {
-            mpu_max = 2; bn_max = 256; groups = (mt + 1) >> 1; ntiles = nt256;
-        }
-        units = static_cast<int64_t>(groups) * ntiles;
-    }
-    __device__ __forceinline__ bool advance_once(int64_t u) {
-        if (e < E && u >= base + units) {
-            base += units;
-            ++e;
-            a_cur = a_nxt;
-            load();
-            return true;
-        }
-        return false;
-    }
-    __device__ bool find(int64_t u, Unit& U) {
-        while (advance_once(u)) {
-        }
-        if (e >= E) return false;
-        const int l = static_cast<int>(u - base);
-        const int g = l / ntiles, n = l - g * ntiles;
-        U.e = e;
-        U.row0 = lo + g * (mpu_max * BM);
-        U.rows = min(mpu_max * BM, rows - g * (mpu_max * BM));
-        U.mpu = (U.rows + BM - 1) / BM;
-        U.n0 = n * bn_max;
-        U.bn = min(bn_max, (De - U.n0 + B_BOX - 1) / B_BOX * B_BOX);
-        U.bn_max = bn_max;
-        U.shared_w = groups > 1;
-        return true;
-    }
-};
-
 // One lane waits; the warp learns the outcome.
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const volatile int* abort,
                                           uint64_t limit) {
@@ -228,6 +187,29 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const v
     ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
     __syncwarp();
     return ok;
+}
+
+// Next unit from the scheduler's queue: 1 = a unit, 0 = no more units,
+// -1 = the wait gave up (abort or time limit). kWarp: every lane of the
+// warp calls this and lane 0 does the barrier traffic.
+template <bool kWarp>
+__device__ __forceinline__ int q_pop(uint32_t qfull0, uint32_t qempty0, const int (*q)[QWORDS],
+                                     Cursor<NQ>& qc, Unit& U, const volatile int* abort,
+                                     uint64_t limit) {
+    const bool ok = kWarp ? warp_wait(qfull0 + 8 * qc.s, qc.ph, abort, limit)
+                          : mbar_wait(qfull0 + 8 * qc.s, qc.ph, abort, limit);
+    if (!ok) return -1;
+    const volatile int* d = q[qc.s];
+    U.e = d[0]; U.row0 = d[1]; U.rows = d[2]; U.mpu = d[3];
+    U.n0 = d[4]; U.bn = d[5]; U.bn_max = d[6]; U.shared_w = d[7] != 0;
+    if (kWarp) {
+        __syncwarp();
+        if (lane_id() == 0) mbar_arrive(qempty0 + 8 * qc.s);
+    } else {
+        mbar_arrive(qempty0 + 8 * qc.s);
+    }
+    qc.next();
+    return U.e >= 0 ? 1 : 0;
 }
 
 __device__ __forceinline__ void fail(volatile int* abort, int32_t* status) {
@@ -317,11 +299,11 @@ __global__ void __launch_bounds__(THREADS, 1)
 
     const uint32_t wfull0 = smem_addr(&ctl->wfull[0]);
     const uint32_t wempty0 = smem_addr(&ctl->wempty[0]);
-    const uint32_t afull0 = smem_addr(&ctl->afull[0]);
-    const uint32_t aempty0 = smem_addr(&ctl->aempty[0]);
     const uint32_t acc_full = smem_addr(&ctl->acc_full);
     const uint32_t acc_empty = smem_addr(&ctl->acc_empty);
     const uint32_t drain = smem_addr(&ctl->drain);
+    const uint32_t qfull0 = smem_addr(&ctl->qfull[0]);
+    const uint32_t qempty0 = smem_addr(&ctl->qempty[0]);
     volatile int* abort = &ctl->abort;
 
     if (threadIdx.x == 0) {
@@ -329,13 +311,13 @@ __global__ void __launch_bounds__(THREADS, 1)
             mbar_init(wfull0 + 8 * s, kGather ? 1 + GATHER_THREADS : 1);
             mbar_init(wempty0 + 8 * s, 1);
         }
-        for (int s = 0; s < A_STAGES; ++s) {
-            mbar_init(afull0 + 8 * s, kGather ? GATHER_THREADS : 1);
-            mbar_init(aempty0 + 8 * s, 1);
-        }
         mbar_init(acc_full, 1);
         mbar_init(acc_empty, EPI_WARPS);
         mbar_init(drain, 1);
+        for (int s = 0; s < NQ; ++s) {
+            mbar_init(qfull0 + 8 * s, 1);
+            mbar_init(qempty0 + 8 * s, (kGather ? GATHER_WARPS : 0) + 2 + EPI_WARPS);
+        }
         ctl->abort = 0;
         fence_barrier_init();
     }
@@ -361,14 +343,18 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int rb = gt >> 3;        // first row of this thread (0..15)
         const uint32_t swz = static_cast<uint32_t>(((c ^ (rb & 7)) << 4));
         const uint64_t pol_x = policy_evict_last();  // rows are re-read by the unit's other n-tiles
-        Walker wk;
-        wk.init(offsets, E, R, De);
+        Cursor<NQ> qc;
         Cursor<W_STAGES> wc;
         Cursor<A_STAGES> ac;
+        Cursor<W_STAGES> back = lag_cursor();  // the K-step A_STAGES back
         bool ok = true, bad = false;
-        for (int64_t u = blockIdx.x; ok; u += gridDim.x) {
+        while (ok) {
             Unit U;
-            if (!wk.find(u, U)) break;
+            const int got = q_pop<true>(qfull0, qempty0, ctl->q, qc, U, abort, limit);
+            if (got <= 0) {
+                if (got < 0 && lane == 0) fail(abort, status);
+                break;
+            }
             const char* src[MAX_MPU][ROWS_PER_THREAD];
 #pragma unroll
             for (int mt = 0; mt < MAX_MPU; ++mt)
@@ -391,7 +377,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 // A slot free means the MMAs of the K-step three back are
                 // done, and with them those of the K-step four back, the last
                 // user of this K-step's W slot (its second half may take m-tile 2).
-                if (!warp_wait(aempty0 + 8 * ac.s, ac.ph ^ 1u, abort, limit)) {
+                if (!warp_wait(wempty0 + 8 * back.s, back.ph, abort, limit)) {
                     if (lane == 0) fail(abort, status);
                     ok = false;
                     break;
@@ -407,11 +393,10 @@ __global__ void __launch_bounds__(THREADS, 1)
                             cp_async_16(dst0 + i * (ROWS_PER_PASS * 128),
                                         nbytes ? src[mt][i] + koff : src[mt][i], nbytes, pol_x);
                 }
-                cp_async_arrive_noinc(afull0 + 8 * ac.s);
                 cp_async_arrive_noinc(wfull0 + 8 * wc.s);
                 ac.next();
                 wc.next();
-                wk.advance_once(u + gridDim.x);  // toward the next unit
+                back.next();
             }
         }
         // Copies still in flight must land before the CTA may exit.
@@ -422,15 +407,19 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (lane == 0) {
             const uint64_t pol_once = policy_evict_first();
             const uint64_t pol_reuse = policy_evict_last();  // also A: re-read by every n-tile
-            Walker wk;
-            wk.init(offsets, E, R, De);
+            Cursor<NQ> qc;
             Cursor<W_STAGES> wc;
             Cursor<A_STAGES> ac;
-            uint32_t w_issued = 0, w_par = 0, a_issued = 0, a_par = 0;
+            Cursor<W_STAGES> back = lag_cursor();
+            uint32_t w_issued = 0, w_par = 0;
             bool ok = true;
-            for (int64_t u = blockIdx.x; ok; u += gridDim.x) {
+            while (ok) {
                 Unit U;
-                if (!wk.find(u, U)) break;
+                const int got = q_pop<false>(qfull0, qempty0, ctl->q, qc, U, abort, limit);
+                if (got <= 0) {
+                    if (got < 0) fail(abort, status);
+                    break;
+                }
                 const int nbox = U.bn / B_BOX;
                 const uint64_t pol = U.shared_w ? pol_reuse : pol_once;
                 // grouped GEMM: m-tiles 0, 1 to the A slot, m-tile 2 to the W slot
@@ -439,14 +428,16 @@ __global__ void __launch_bounds__(THREADS, 1)
                                      (!kGather && U.mpu > 2 ? static_cast<uint32_t>(A_BYTES) : 0u);
                 const uint32_t atx = static_cast<uint32_t>(a_lo * A_BYTES);
                 for (int ks = 0; ks < nk; ++ks) {
-                    if (!mbar_wait(wempty0 + 8 * wc.s, wc.ph ^ 1u, abort, limit) ||
-                        (!kGather && !mbar_wait(aempty0 + 8 * ac.s, ac.ph ^ 1u, abort, limit))) {
+                    // W slot: free once the K-step W_STAGES back is done; grouped
+                    // GEMM (A by TMA as well): once the one A_STAGES back is done.
+                    if (!(kGather ? mbar_wait(wempty0 + 8 * wc.s, wc.ph ^ 1u, abort, limit)
+                                  : mbar_wait(wempty0 + 8 * back.s, back.ph, abort, limit))) {
                         fail(abort, status);
                         ok = false;
                         break;
                     }
                     const uint32_t wfull = wfull0 + 8 * wc.s;
-                    mbar_arrive_expect_tx(wfull, wtx);
+                    mbar_arrive_expect_tx(wfull, kGather ? wtx : wtx + atx);
                     const uint32_t wsl = sbase + wc.s * W_SLOT;
                     for (int b = 0; b < nbox; ++b) {
                         // bf16: 64 columns x 64 K rows (MN-major); FP8: 128 K codes x 64
@@ -461,31 +452,24 @@ __global__ void __launch_bounds__(THREADS, 1)
                     w_issued |= 1u << wc.s;
                     w_par = (w_par & ~(1u << wc.s)) | (wc.ph << wc.s);
                     if (!kGather) {  // rows past the expert's end are loaded but never stored
-                        const uint32_t afull = afull0 + 8 * ac.s;
-                        mbar_arrive_expect_tx(afull, atx);
                         for (int mt = 0; mt < U.mpu; ++mt)
                             tma_load_2d(a_tile(wc.s, ac.s, mt), &amap, ks * BKE, U.row0 + mt * BM,
-                                        mt < 2 ? afull : wfull, pol_reuse);
-                        a_issued |= 1u << ac.s;
-                        a_par = (a_par & ~(1u << ac.s)) | (ac.ph << ac.s);
+                                        wfull, pol_reuse);
                     }
                     wc.next();
                     ac.next();
-                    wk.advance_once(u + gridDim.x);  // toward the next unit
+                    back.next();
                 }
             }
             // Every copy this thread started must land before the CTA may exit.
             for (int s = 0; s < W_STAGES; ++s)
                 if ((w_issued >> s) & 1u) mbar_wait(wfull0 + 8 * s, (w_par >> s) & 1u, nullptr, limit);
-            for (int s = 0; s < A_STAGES; ++s)
-                if ((a_issued >> s) & 1u) mbar_wait(afull0 + 8 * s, (a_par >> s) & 1u, nullptr, limit);
         }
         __syncwarp();
     } else if (warp == MMA_WARP) {
         // ----------------------------------------------------------- MMA
         if (lane == 0) {
-            Walker wk;
-            wk.init(offsets, E, R, De);
+            Cursor<NQ> qc;
             Cursor<W_STAGES> wc;
             Cursor<A_STAGES> ac;
             uint32_t acc_phase = 0;
@@ -501,9 +485,13 @@ __global__ void __launch_bounds__(THREADS, 1)
             const uint64_t b_desc0 = kFp8 ? sdesc_sw128(0, 16, 1024)
                                           : sdesc_sw128(0, B_BOX_BYTES, 1024);
             constexpr uint32_t b_step = kFp8 ? (32 >> 4) : ((UMMA_K * 128) >> 4);
-            for (int64_t u = blockIdx.x; ok; u += gridDim.x) {
+            while (ok) {
                 Unit U;
-                if (!wk.find(u, U)) break;
+                const int got = q_pop<false>(qfull0, qempty0, ctl->q, qc, U, abort, limit);
+                if (got <= 0) {
+                    if (got < 0) fail(abort, status);
+                    break;
+                }
                 if (!mbar_wait(acc_empty, acc_phase ^ 1u, abort, limit)) {
                     fail(abort, status);
                     break;
@@ -514,8 +502,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 const int mpu = U.mpu;
                 const uint32_t acc_stride = static_cast<uint32_t>(U.bn_max);
                 for (int ks = 0; ks < nk; ++ks) {
-                    if (!mbar_wait(wfull0 + 8 * wc.s, wc.ph, abort, limit) ||
-                        !mbar_wait(afull0 + 8 * ac.s, ac.ph, abort, limit)) {
+                    if (!mbar_wait(wfull0 + 8 * wc.s, wc.ph, abort, limit)) {
                         fail(abort, status);
                         ok = false;
                         break;
@@ -539,10 +526,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                         }
                     }
                     mma_commit(wempty0 + 8 * wc.s);
-                    mma_commit(aempty0 + 8 * ac.s);
                     wc.next();
                     ac.next();
-                    wk.advance_once(u + gridDim.x);  // toward the next unit, behind the MMAs
                 }
                 if (!ok) break;
                 mma_commit(acc_full);
@@ -557,12 +542,15 @@ __global__ void __launch_bounds__(THREADS, 1)
         // ------------------------------------------------------ epilogue
         const int q = warp;  // TMEM lane quarter this warp may access (warps 0..3)
         const bool wide = (De % 16) == 0 && (reinterpret_cast<uintptr_t>(out) & 31u) == 0;
-        Walker wk;
-        wk.init(offsets, E, R, De);
+        Cursor<NQ> qc;
         uint32_t acc_phase = 0;
-        for (int64_t u = blockIdx.x;; u += gridDim.x) {
+        while (true) {
             Unit U;
-            if (!wk.find(u, U)) break;
+            const int got = q_pop<true>(qfull0, qempty0, ctl->q, qc, U, abort, limit);
+            if (got <= 0) {
+                if (got < 0 && lane == 0) fail(abort, status);
+                break;
+            }
             // FP8: this lane's row scales (one per m-tile) and column scales
             // (one per 32 columns), loaded while the unit's MMAs still run.
             float rs_pre[MAX_MPU] = {1.0f, 1.0f, 1.0f};
@@ -647,7 +635,88 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
     }
 
-    // (warp 8 has no role and comes straight here)
+    if (warp == SCHED_WARP) {
+        // --------------------------------------------------------- scheduler
+        // Walks the unit numbering for this CTA (units blockIdx.x, +gridDim.x,
+        // ...) 32 experts at a time, one expert per lane, and queues each
+        // unit's descriptor; a descriptor with e = -1 ends the list.
+        const int nt256 = (De + 255) >> 8, nt128 = (De + 127) >> 7;
+        int e0 = -32;
+        int64_t before = 0, total = 0, cum = 0, units = 0;
+        int lo = 0, rows = 0, mpu_max = 2, bn_max = 256, groups = 0, ntiles = 1;
+        Cursor<NQ> qc;
+        for (int64_t u = blockIdx.x;; u += gridDim.x) {
+            bool have = false;
+            while (true) {
+                if (e0 >= 0 && u < before + total) {
+                    have = true;
+                    break;
+                }
+                if (e0 >= 0) before += total;
+                e0 += 32;
+                if (e0 >= E) break;
+                const int e = e0 + lane;
+                units = 0;
+                rows = 0;
+                if (e < E) {
+                    lo = min(max(__ldg(offsets + e), 0), R);
+                    const int hi = min(max(__ldg(offsets + e + 1), 0), R);
+                    rows = max(hi, lo) - lo;
+                    const int mt = (rows + BM - 1) / BM;
+                    if (mt == 3) {
+                        mpu_max = 3; bn_max = 128; groups = 1; ntiles = nt128;
+                    } else {
+                        mpu_max = 2; bn_max = 256; groups = (mt + 1) >> 1; ntiles = nt256;
+                    }
+                    units = static_cast<int64_t>(groups) * ntiles;
+                }
+                cum = units;
+#pragma unroll
+                for (int d = 1; d < 32; d <<= 1) {
+                    const int64_t t = __shfl_up_sync(0xffffffffu, cum, d);
+                    if (lane >= d) cum += t;
+                }
+                total = __shfl_sync(0xffffffffu, cum, 31);
+            }
+            int d[QWORDS] = {-1, 0, 0, 0, 0, 0, 0, 0};
+            if (have) {
+                const int64_t l = u - before;
+                const int s = __ffs(__ballot_sync(0xffffffffu, l < cum)) - 1;
+                const int s_lo = __shfl_sync(0xffffffffu, lo, s);
+                const int s_rows = __shfl_sync(0xffffffffu, rows, s);
+                const int s_mpu = __shfl_sync(0xffffffffu, mpu_max, s);
+                const int s_bn = __shfl_sync(0xffffffffu, bn_max, s);
+                const int s_groups = __shfl_sync(0xffffffffu, groups, s);
+                const int s_nt = __shfl_sync(0xffffffffu, ntiles, s);
+                const int64_t s_first = __shfl_sync(0xffffffffu, cum - units, s);
+                const int li = static_cast<int>(l - s_first);
+                const int g = li / s_nt, n = li - g * s_nt;
+                d[0] = e0 + s;
+                d[1] = s_lo + g * (s_mpu * BM);
+                d[2] = min(s_mpu * BM, s_rows - g * (s_mpu * BM));
+                d[3] = (d[2] + BM - 1) / BM;
+                d[4] = n * s_bn;
+                d[5] = min(s_bn, (De - d[4] + B_BOX - 1) / B_BOX * B_BOX);
+                d[6] = s_bn;
+                d[7] = s_groups > 1 ? 1 : 0;
+            }
+            bool ok = true;
+            if (lane == 0) {
+                ok = mbar_wait(qempty0 + 8 * qc.s, qc.ph ^ 1u, abort, limit);
+                if (ok) {
+#pragma unroll
+                    for (int i = 0; i < QWORDS; ++i) ctl->q[qc.s][i] = d[i];
+                    mbar_arrive(qfull0 + 8 * qc.s);
+                } else {
+                    fail(abort, status);
+                }
+            }
+            ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+            qc.next();
+            if (!have || !ok) break;
+        }
+    }
+    // (every role comes here when done)
     tc_fence_before_sync();
     __syncthreads();
     if (warp == MMA_WARP) {
