@@ -105,6 +105,25 @@ def workload_bytes(wl, counts: np.ndarray) -> dict:
     }
 
 
+def binding_roofline(flops: float, alg_bytes: float, kernel_ms: float, peaks: dict,
+                     tensor_peak: float | None = None) -> dict:
+    """Roofline of one GEMM launch: the slower of its FLOPs at the tensor peak
+    and its algorithmic bytes at the HBM peak binds; `frac` is that time over
+    the measured kernel time (= achieved / peak in the binding unit)."""
+    tp = tensor_peak or peaks["bf16_tflops"]
+    t_tensor = flops / (tp * 1e12) * 1e3
+    t_hbm = alg_bytes / (peaks["hbm_gbs"] * 1e9) * 1e3
+    sec = kernel_ms * 1e-3
+    hbm = {"achieved": alg_bytes / sec / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+           "frac": t_hbm / kernel_ms, "ms": t_hbm}
+    tensor = {"achieved": flops / sec / 1e12, "peak": tp, "unit": "TFLOP/s",
+              "frac": t_tensor / kernel_ms, "ms": t_tensor}
+    b = hbm if t_hbm >= t_tensor else tensor
+    return {"bound": "hbm" if b is hbm else "tensor", "achieved": b["achieved"], "peak": b["peak"],
+            "unit": b["unit"], "frac": b["frac"], "roofline_ms": max(t_hbm, t_tensor),
+            "kernel_ms": kernel_ms, "hbm": hbm, "tensor": tensor}
+
+
 def config_of(wl) -> dict:
     return {
         "workload": f"{wl.name}: T={wl.T} D={wl.D} E={wl.E} top_k={wl.k} D_expert={wl.De}"
@@ -403,16 +422,23 @@ def run_ours(args, wl):
         raise RuntimeError("device status set during the end-to-end run")
     del pipe
 
+    peaks, peak_kind = load_peaks()
+    # the other workloads, each with its own binding roofline and oracle sample
+    others = {}
+    if rank == 0 and not args.no_others:
+        for name in OTHER_WORKLOADS:
+            if name != wl.name:
+                others[name] = measure_other(args, ig.WORKLOADS[name], wl, x, W, dev, stream,
+                                             peaks, peak_kind)
     if sampler:
         sampler.stop()
     if rank != 0:
         return None
 
-    peaks, peak_kind = load_peaks()
     b = workload_bytes(wl, counts)
     alg_bytes = b["x_gathered"] + b["w_touched"] + b["out"] + b["indices"]
-    achieved_gbs = alg_bytes / (gemm_avg_ms * 1e-3) / 1e9
-    gemm_tflops = flops / (gemm_avg_ms * 1e-3) / 1e12
+    roof = binding_roofline(flops, alg_bytes, gemm_avg_ms, peaks)
+    roof["tensor"]["peak_sustained"] = peaks.get("bf16_tflops_sustained")
     value = world * flops / (step_ms * 1e-3) / 1e12
     kernel = "pair" if args.gemm_kernel == "pair" else "single"
     traffic = profiled_traffic(wl.name, kernel)
@@ -422,16 +448,12 @@ def run_ours(args, wl):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
         "warmup": max(3, args.warmup), "ms_per_step": step_ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": dict(config_of(wl), gemm_kernel=kernel),
+        "config": config_of(wl),
+        "gemm_kernel": kernel,
         "pct_bf16_peak": 100.0 * value / world / peaks["bf16_tflops"],
-        "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": peaks["hbm_gbs"],
-                     "unit": "GB/s", "frac": achieved_gbs / peaks["hbm_gbs"],
-                     "traffic": traffic, "peak_kind": peak_kind,
-                     "kernel": GEMM_KERNELS[kernel][2], "kernel_ms": gemm_avg_ms,
-                     "algorithmic_bytes": alg_bytes, "bytes_breakdown": b,
-                     "tensor": {"achieved": gemm_tflops, "peak": peaks["bf16_tflops"],
-                                "peak_sustained": peaks.get("bf16_tflops_sustained"),
-                                "unit": "TFLOP/s", "frac": gemm_tflops / peaks["bf16_tflops"]}},
+        "roofline": dict(roof, traffic=traffic, peak_kind=peak_kind,
+                         kernel=GEMM_KERNELS[kernel][2], algorithmic_bytes=alg_bytes,
+                         bytes_breakdown=b),
         "kernel_share": {GEMM_KERNELS[kernel][2]: gemm_avg_ms / step_ms},
         "cpu_baseline": {"value": cpu_value, "unit": UNIT, "cores": os.cpu_count() or 1,
                          "kind": "oracle",
@@ -448,7 +470,77 @@ def run_ours(args, wl):
     }
     if l2_warm is not None:
         line["l2_warm"] = l2_warm
+    if others:
+        line["workloads"] = others
     return line
+
+
+# Workloads reported beside the headline one in the default bench line.
+OTHER_WORKLOADS = ("tiny", "mid", "skew", "decode")
+
+
+def measure_other(args, wl, head_wl, head_x, head_W, dev, stream, peaks, peak_kind):
+    """One workload's step (route + dispatch GEMM) on resident inputs: CUDA-event
+    times, binding roofline and a short oracle CPU sample. Workloads with the
+    headline's weight shape and seed reuse its device W (the generator makes
+    the same bytes), and the same x rows when D and the seed agree."""
+    import torch
+    import inputgen as ig
+    import moe_token_dispatch_gb300 as pk
+
+    def to_dev(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
+
+    same_w = (wl.E, wl.D, wl.De, wl.seed) == (head_wl.E, head_wl.D, head_wl.De, head_wl.seed)
+    same_x = (wl.D, wl.seed) == (head_wl.D, head_wl.seed) and wl.T <= head_wl.T
+    x_host = ig.make_x(wl)
+    topk_host = ig.make_topk(wl)
+    x = head_x[: wl.T] if same_x else to_dev(x_host)
+    W = head_W if same_w else to_dev(ig.make_W(wl))
+    topk = torch.from_numpy(topk_host).to(dev)
+    md = pk.MoeDispatch(wl.T, wl.k, wl.E, wl.D, wl.De, device=dev, with_inv_perm=True)
+    flush = None
+    if wl.E * wl.D * wl.De * 2 <= 256e6:
+        flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    K = max(1, min(args.steps, 50))
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    for i in range(max(3, args.warmup) + K):
+        e = ev[i - max(3, args.warmup)] if i >= max(3, args.warmup) else None
+        if e:
+            e[0].record(stream)
+        md.route(topk, stream)
+        if e:
+            e[1].record(stream)
+        md.gemm(x, W, stream)
+        if e:
+            e[2].record(stream)
+            e[3].record(stream)
+        if flush is not None:
+            flush.fill_(1)
+    torch.cuda.synchronize()
+    if md.status_code() != 0:
+        raise RuntimeError(f"device status {pk.pk_status_str(md.status_code())} ({wl.name})")
+    step_ms = sum(e[0].elapsed_time(e[3]) for e in ev) / K
+    gemm_ms = sum(e[1].elapsed_time(e[2]) for e in ev) / K
+    counts = md.counts.cpu().numpy()
+    b = workload_bytes(wl, counts)
+    alg_bytes = b["x_gathered"] + b["w_touched"] + b["out"] + b["indices"]
+    flops = float(wl.flops)
+    roof = binding_roofline(flops, alg_bytes, gemm_ms, peaks)
+    case = ig.Case(wl, x_host, topk_host, None)
+    cpu_value, cpu_info = oracle_sample(case, wl, args.cpu_seconds_other, os.cpu_count() or 1)
+    del md, flush
+    return {
+        "config": config_of(wl), "steps": K, "ms_per_step": step_ms,
+        "value": flops / (step_ms * 1e-3) / 1e12, "unit": UNIT,
+        "pct_bf16_peak": 100.0 * flops / (step_ms * 1e-3) / 1e12 / peaks["bf16_tflops"],
+        "roofline": dict(roof, peak_kind=peak_kind, kernel="k_dispatch_gemm",
+                         algorithmic_bytes=alg_bytes, flops=flops, bytes_breakdown=b),
+        "cpu_baseline": {"value": cpu_value, "unit": UNIT, "cores": os.cpu_count() or 1,
+                         "kind": "oracle",
+                         "sample": f"full routing + float64 GEMM of {cpu_info['rows']} random "
+                                   f"sorted rows of {wl.R} ({cpu_info['seconds']:.1f} s)"},
+    }
 
 
 def run_op(args, wl):
@@ -601,6 +693,10 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="ep")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--cpu-seconds-other", type=float, default=3.0,
+                    help="oracle CPU sample per additional workload")
+    ap.add_argument("--no-others", action="store_true",
+                    help="time only the headline workload")
     ap.add_argument("--gemm-kernel", choices=["auto", "single", "pair"], default="auto",
                     help="dispatch GEMM kernel: auto (= single), single (one CTA per SM) or pair "
                          "(2-CTA clusters)")

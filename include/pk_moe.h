@@ -328,6 +328,21 @@ void pk_moe_set_wait_limit_ns(uint64_t limit_ns);
  */
 int pk_debug_bounded_wait(int32_t* status_word, uint64_t limit_ns, void* stream);
 
+/*
+ * Failure-detection check of the GEMM pipeline itself (off by default). While
+ * set, every launch of the one-CTA dispatch or grouped GEMM kernel has CTA
+ * `cta` arm K-step `kstep` of its own sequence (its units in order, nk K-steps
+ * each) without issuing that K-step's weight (and grouped-GEMM row) copies, so
+ * the K-step's full barrier never completes: the MMA thread's bounded wait
+ * runs out, writes PK_ERR_TIMEOUT to the status word and raises the CTA's
+ * abort flag, every role leaves its loop (each waits for the copies it has in
+ * flight, the MMA thread for its issued MMAs), TMEM is freed and the kernel
+ * returns. Outputs of that launch are undefined. cta < 0 or kstep < 0 turns
+ * it off. Not thread-safe with concurrent launches; meant for tests, together
+ * with a short pk_moe_set_wait_limit_ns.
+ */
+void pk_debug_stall_gemm(int32_t cta, int64_t kstep);
+
 #ifdef __cplusplus
 }
 #endif

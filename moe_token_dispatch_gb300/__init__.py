@@ -25,6 +25,7 @@ from ._binding import (  # noqa: F401
     lib,
     pk_abi_version,
     pk_debug_bounded_wait,
+    pk_debug_stall_gemm,
     pk_moe_build_perm,
     pk_moe_combine,
     pk_moe_dispatch_gemm,

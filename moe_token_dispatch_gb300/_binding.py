@@ -78,6 +78,8 @@ def _load():
     lib.pk_moe_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
     lib.pk_debug_bounded_wait.restype = ctypes.c_int
     lib.pk_debug_bounded_wait.argtypes = [P, ctypes.c_uint64, P]
+    lib.pk_debug_stall_gemm.restype = None
+    lib.pk_debug_stall_gemm.argtypes = [I32, ctypes.c_int64]
     return lib
 
 
@@ -309,3 +311,9 @@ def pk_debug_bounded_wait(status_word: torch.Tensor, limit_ns: int, stream=None)
     rc = lib.pk_debug_bounded_wait(_ptr(status_word, torch.int32, "status_word", 1), int(limit_ns),
                                    _stream(stream))
     _check(rc, "pk_debug_bounded_wait")
+
+
+def pk_debug_stall_gemm(cta: int, kstep: int) -> None:
+    """Test hook: CTA `cta` of each one-CTA GEMM launch skips the copies of its
+    K-step `kstep`; a negative value turns it off."""
+    lib.pk_debug_stall_gemm(int(cta), int(kstep))

@@ -218,6 +218,8 @@ void pk_moe_set_wait_limit_ns(uint64_t limit_ns) {
     g_wait_limit_ns.store(limit_ns ? limit_ns : kDefaultWaitLimitNs, std::memory_order_relaxed);
 }
 
+void pk_debug_stall_gemm(int32_t cta, int64_t kstep) { pk::set_debug_stall(cta, kstep); }
+
 int pk_debug_bounded_wait(int32_t* status_word, uint64_t limit_ns, void* stream) {
     if (!status_word || limit_ns == 0) return PK_ERR_INVALID_ARG;
     cudaError_t err =

@@ -272,7 +272,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                     const float* __restrict__ sw,
                     const int32_t* __restrict__ perm, const int32_t* __restrict__ offsets,
                     uint16_t* __restrict__ out, int32_t T, int32_t k, int32_t D, int32_t E,
-                    int32_t De, int32_t* status, uint64_t limit) {
+                    int32_t De, int32_t* status, uint64_t limit, int64_t stall) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t sbase = (raw + 1023u) & ~1023u;
@@ -413,6 +413,12 @@ __global__ void __launch_bounds__(THREADS, 1)
             Cursor<W_STAGES> back = lag_cursor();
             uint32_t w_issued = 0, w_par = 0;
             bool ok = true;
+            // Failure-detection test hook (off: stall < 0): CTA stall >> 40 arms
+            // K-step (stall & 2^40-1) of its sequence but issues none of its
+            // copies, so that K-step's full barrier never completes.
+            const int64_t stall_step =
+                (stall >= 0 && (stall >> 40) == blockIdx.x) ? (stall & ((int64_t{1} << 40) - 1)) : -1;
+            int64_t kcount = 0;
             while (ok) {
                 Unit U;
                 const int got = q_pop<false>(qfull0, qempty0, ctl->q, qc, U, abort, limit);
@@ -439,7 +445,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                     const uint32_t wfull = wfull0 + 8 * wc.s;
                     mbar_arrive_expect_tx(wfull, kGather ? wtx : wtx + atx);
                     const uint32_t wsl = sbase + wc.s * W_SLOT;
-                    for (int b = 0; b < nbox; ++b) {
+                    const bool stalled = kcount++ == stall_step;
+                    for (int b = 0; b < nbox && !stalled; ++b) {
                         // bf16: 64 columns x 64 K rows (MN-major); FP8: 128 K codes x 64
                         // columns (K-major). Either way box b lands 8 KiB further.
                         if (kFp8)
@@ -449,9 +456,11 @@ __global__ void __launch_bounds__(THREADS, 1)
                             tma_load_3d(wsl + b * B_BOX_BYTES, &wmap, U.n0 + b * B_BOX, ks * BKE,
                                         U.e, wfull, pol);
                     }
-                    w_issued |= 1u << wc.s;
-                    w_par = (w_par & ~(1u << wc.s)) | (wc.ph << wc.s);
-                    if (!kGather) {  // rows past the expert's end are loaded but never stored
+                    if (!stalled) {
+                        w_issued |= 1u << wc.s;
+                        w_par = (w_par & ~(1u << wc.s)) | (wc.ph << wc.s);
+                    }
+                    if (!kGather && !stalled) {  // rows past the expert's end are loaded but never stored
                         for (int mt = 0; mt < U.mpu; ++mt)
                             tma_load_2d(a_tile(wc.s, ac.s, mt), &amap, ks * BKE, U.row0 + mt * BM,
                                         wfull, pol_reuse);
@@ -731,6 +740,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 namespace {
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::atomic<int64_t> g_debug_stall{-1};
 std::once_flag g_encode_once;
 
 struct DevInfo {
@@ -798,6 +808,7 @@ int launch_common(bool gather, bool fp8, const void* A, const float* sx, const i
                   const int32_t* offsets, const void* W, const float* sw, int32_t T, int32_t k,
                   int32_t D, int32_t E, int32_t De, uint16_t* out, int32_t* status,
                   cudaStream_t stream, uint64_t wait_limit_ns) {
+    const int64_t stall = g_debug_stall.load(std::memory_order_relaxed);
     using namespace dg;
     auto enc = encoder();
     if (!enc) return PK_ERR_CUDA;
@@ -850,18 +861,18 @@ int launch_common(bool gather, bool fp8, const void* A, const float* sx, const i
     const uint8_t* a8 = static_cast<const uint8_t*>(A);
     if (fp8 && gather)
         k_dispatch_gemm<true, true><<<sms, THREADS, SMEM_BYTES, stream>>>(
-            wmap, amap, a8, sx, sw, perm, offsets, out, T, k, D, E, De, status, wait_limit_ns);
+            wmap, amap, a8, sx, sw, perm, offsets, out, T, k, D, E, De, status, wait_limit_ns, stall);
     else if (fp8)
         k_dispatch_gemm<false, true><<<sms, THREADS, SMEM_BYTES, stream>>>(
-            wmap, amap, a8, sx, sw, nullptr, offsets, out, T, k, D, E, De, status, wait_limit_ns);
+            wmap, amap, a8, sx, sw, nullptr, offsets, out, T, k, D, E, De, status, wait_limit_ns, stall);
     else if (gather)
         k_dispatch_gemm<true, false><<<sms, THREADS, SMEM_BYTES, stream>>>(
             wmap, amap, a8, nullptr, nullptr, perm, offsets, out, T, k, D, E, De, status,
-            wait_limit_ns);
+            wait_limit_ns, stall);
     else
         k_dispatch_gemm<false, false><<<sms, THREADS, SMEM_BYTES, stream>>>(
             wmap, amap, a8, nullptr, nullptr, perm, offsets, out, T, k, D, E, De, status,
-            wait_limit_ns);
+            wait_limit_ns, stall);
     return cudaGetLastError() == cudaSuccess ? PK_OK : PK_ERR_CUDA;
 }
 
@@ -882,6 +893,13 @@ int launch_dispatch_gemm_fp8_single(const uint8_t* xq, const float* sx, const in
                                     uint64_t wait_limit_ns) {
     return launch_common(true, true, xq, sx, perm, offsets, wq, sw, T, k, D, E, De, out, status,
                          stream, wait_limit_ns);
+}
+
+void set_debug_stall(int32_t cta, int64_t kstep) {
+    g_debug_stall.store(cta >= 0 && kstep >= 0 && kstep < (int64_t{1} << 40)
+                            ? (static_cast<int64_t>(cta) << 40) | kstep
+                            : -1,
+                        std::memory_order_relaxed);
 }
 
 int launch_grouped_gemm(const uint16_t* A, const int32_t* offsets, const uint16_t* W, int32_t R,

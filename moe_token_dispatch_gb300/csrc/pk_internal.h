@@ -68,6 +68,9 @@ int launch_grouped_gemm(const uint16_t* A, const int32_t* offsets, const uint16_
                         cudaStream_t stream, uint64_t wait_limit_ns);
 
 cudaError_t launch_bounded_wait_probe(int32_t* status, uint64_t limit_ns, cudaStream_t stream);
+// Test hook of the one-CTA GEMM kernels: CTA `cta` skips the copies of its
+// K-step `kstep` (counted over its units); cta < 0 turns it off.
+void set_debug_stall(int32_t cta, int64_t kstep);
 
 cudaError_t launch_router_topk(const float* logits, int32_t T, int32_t E, int32_t k,
                                int32_t* topk, float* gates, cudaStream_t stream);

@@ -102,3 +102,26 @@ def test_committed_profiles_carry_hash_and_traffic():
         assert re.search(r"kernel_source_sha256_16: [0-9a-f]{16}", text), name
         assert re.search(r"traffic_bytes_per_launch: [0-9.eE+]+", text), name
         assert "ncu " in text and "--clock-control none" in text, name
+
+
+def test_binding_roofline_picks_the_slower_limit():
+    peaks = {"hbm_gbs": 1000.0, "bf16_tflops": 100.0}
+    # 1 GB at 1000 GB/s = 1 ms; 50 TFLOP at 100 TFLOP/s = 0.5 s: tensor binds
+    r = bench.binding_roofline(50e12, 1e9, 1000.0, peaks)
+    assert r["bound"] == "tensor" and r["unit"] == "TFLOP/s"
+    assert abs(r["frac"] - 0.5) < 1e-12 and abs(r["roofline_ms"] - 500.0) < 1e-9
+    assert abs(r["achieved"] - 50.0) < 1e-9 and r["peak"] == 100.0
+    # 10 GB (10 ms at HBM) against 0.1 TFLOP (1 ms): HBM binds; kernel took 20 ms
+    r = bench.binding_roofline(1e11, 1e10, 20.0, peaks)
+    assert r["bound"] == "hbm" and r["unit"] == "GB/s"
+    assert abs(r["frac"] - 0.5) < 1e-12 and abs(r["achieved"] - 500.0) < 1e-9
+    assert abs(r["tensor"]["frac"] - 0.05) < 1e-12
+
+
+def test_both_arms_describe_the_workload_alike():
+    # the reference arm and ours print config_of(wl) unchanged
+    import inspect
+    src = inspect.getsource(bench.run_ours)
+    assert '"config": config_of(wl),' in src
+    assert '"config": config_of(wl),' in inspect.getsource(bench.run_reference)
+    assert set(bench.OTHER_WORKLOADS) == {"tiny", "mid", "skew", "decode"}

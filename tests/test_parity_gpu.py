@@ -196,6 +196,55 @@ def test_bounded_wait_times_out_and_context_survives(gpu_lib):
     check_case(pk, x, topk, W, 2)
 
 
+@pytest.mark.parametrize("grouped", [False, True])
+def test_gemm_pipeline_timeout_drains_every_role(gpu_lib, grouped):
+    """A K-step whose copies are never issued (test hook on CTA 0) makes the
+    MMA thread's bounded wait run out inside the real pipeline: the launch
+    ends by itself with PK_ERR_TIMEOUT, every role has left its loop (the
+    producers and dispatch warps are blocked on slots that the stalled K-step
+    never frees, so they leave through the abort flag), TMEM was freed, and
+    the next launches on the same context run normally."""
+    pk = gpu_lib
+    pk.pk_moe_set_gemm_kernel(pk.PK_GEMM_KERNEL_SINGLE)
+    # 64 experts x 8 n-tiles of 256 columns, 8 K-steps each: CTA 0 owns several
+    # units, so its producers fill the ring past the stalled K-step and block.
+    T, D, E, k, De = 256, 512, 64, 2, 2048
+    x, topk, W = _case(T, D, E, k, De)
+    Wd = u16_to_bf16_dev(W)
+    md = pk.MoeDispatch(T, k, E, D, De)
+    xd = u16_to_bf16_dev(x)
+    md.route(torch.from_numpy(topk).cuda())
+    torch.cuda.synchronize()
+    assert md.status_code() == 0
+    a_sorted = xd[(md.perm[: T * k] // k).long()].contiguous() if grouped else None
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    pk.pk_moe_set_wait_limit_ns(50_000_000)  # 50 ms
+    pk.pk_debug_stall_gemm(0, 2)
+    try:
+        t0.record()
+        if grouped:
+            pk.pk_moe_grouped_gemm(a_sorted, md.offsets, Wd, md.out, md.status)
+        else:
+            md.gemm(xd, Wd)
+        t1.record()
+        torch.cuda.synchronize()
+    finally:
+        pk.pk_debug_stall_gemm(-1, -1)
+        pk.pk_moe_set_wait_limit_ns(0)   # back to the default limit
+        pk.pk_moe_set_gemm_kernel(pk.PK_GEMM_KERNEL_AUTO)
+    assert md.status_code() == pk.PK_ERR_TIMEOUT
+    ms = t0.elapsed_time(t1)
+    assert 40.0 <= ms < 1000.0, ms
+    # the same context runs the path again, and the same launch is correct
+    md.clear_status()
+    check_case(pk, x, topk, W, E, rows=boundary_rows(oracle.route_counts(topk, E)[1],
+                                                       np.random.default_rng(2), 64),
+               W_dev=Wd)
+    xs, tks, Ws = _case(64, 64, 2, 1, 64)
+    check_case(pk, xs, tks, Ws, 2)
+
+
 # ------------------------------------------------- the five named workloads
 def test_mid_workload(gpu_lib, gemm_kernel):
     wl = ig.WORKLOADS["mid"]
