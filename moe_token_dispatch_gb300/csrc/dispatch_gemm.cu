@@ -5,7 +5,7 @@
 // their intra-SM overlap (section "Using the Right Overlapping Schedule"):
 // producer warps move tiles while the tensor cores stay busy.
 //
-// Persistent kernel, one CTA per SM, 11 warps:
+// Persistent kernel, one CTA per SM, 12 warps:
 //   warps 0-3  epilogue: tcgen05.ld of the warp's TMEM lane quarter, bf16
 //              round-to-nearest-even, masked 16-byte stores of valid rows and
 //              columns.
@@ -16,27 +16,32 @@
 //   warp 5     W producer (one thread): per K-step of 64 rows, TMA-loads the
 //              W_e tile [64 x bn] as 64x64 boxes, 128-byte swizzle (MN-major
 //              operand).
-//   warps 6,7,9,10  dispatch: gather the unit's routed x rows with 16-byte
-//              cp.async into K-major 128-byte-swizzled tiles (each warp
-//              instruction moves four whole 128-byte row segments); each
-//              thread's copies arrive on the K-step's full barrier when they
-//              land, and the MMA thread fences them into the async proxy after
-//              its wait, before the tensor cores read them.
+//   warps 6,7,9,10  dispatch: gather the routed x rows of the unit's m-tiles
+//              0 and 1 with 16-byte cp.async into K-major 128-byte-swizzled
+//              tiles (each warp instruction moves four whole 128-byte row
+//              segments); each thread's copies arrive on the K-step's full
+//              barrier when they land, and the MMA thread fences them into the
+//              async proxy after its wait, before the tensor cores read them.
+//   warp 11    dispatch of m-tile 2 of 3-m-tile units, the same way.
 //   warp 8     scheduler: walks this CTA's units 32 experts at a time (one
 //              expert per lane) and queues each unit's shape in shared memory
 //              (eight entries, full/empty barriers), so no other role walks
 //              the expert offsets. Warps share an SM sub-partition with the
 //              warps whose index is equal mod 4; this keeps the busy gather
 //              warps off the MMA issuer's sub-partition.
-// Two rings of shared-memory slots connect producers and MMA: four 32 KiB W
-// slots and three 32 KiB A slots, one of each per K-step. W comes from HBM
-// and takes longest to arrive, so it runs up to four K-steps ahead; the
-// gathered rows mostly hit L2 and run three ahead. One full and one empty
-// barrier per K-step (indexed by the W slot) serve both rings: the full
-// barrier counts the W bytes and every gather thread's arrival, so the MMA
-// thread waits once per K-step, and its one commit frees both slots (a
-// producer of the A ring waits for the K-step three back, which also frees
-// the W slot four back).
+// Two rings of shared-memory slots connect producers and MMA: three 32 KiB W
+// slots and four 32 KiB A slots (m-tiles 0 and 1), one of each per K-step; a
+// 3-m-tile unit puts its m-tile 2 in the second half of its W slot (its W
+// tile is 16 KiB). The ring that bounds the K-loop is the gathered rows':
+// measured on ep, one A slot less costs 31 %, one W slot less nothing. So
+// the A ring runs four K-steps ahead and the W ring three. One full and one
+// empty barrier per K-step (a ring of eight pairs, indexed by K-step)
+// serve both rings: the full barrier counts the W bytes and every gather
+// thread's arrival, so the MMA thread waits once per K-step, and its one
+// commit frees both slots; each producer waits for the K-step that last used
+// its slot. m-tile 2 has a warp of its own because a thread's cp.async
+// arrivals cover all its earlier copies: with the shorter lead of the W slot
+// it would hold back the arrivals of m-tiles 0 and 1.
 //
 // The same kernel, instantiated with kGather = false, is the grouped GEMM of
 // rows that are already in expert order (the down-projection that follows the
@@ -92,27 +97,31 @@ constexpr int A_BYTES = BM * BK * 2;         // 16 KiB per m-tile
 // ahead of the tensor cores (HBM latency), the A ring three (gathered rows).
 // A W slot holds the W tile (bn_max x 128 B); 3-m-tile units (bn_max = 128)
 // put their third A tile in its second half. An A slot holds m-tiles 0, 1.
-constexpr int W_STAGES = 4;
-constexpr int A_STAGES = 3;
+constexpr int W_STAGES = 3;
+constexpr int A_STAGES = 4;
 constexpr int W_SLOT = 32 * 1024;
 constexpr int A_SLOT = 2 * A_BYTES;
-constexpr int A_RING_OFF = W_STAGES * W_SLOT;                // 128 KiB
+constexpr int A_RING_OFF = W_STAGES * W_SLOT;                // 96 KiB
 constexpr int RING_BYTES = A_RING_OFF + A_STAGES * A_SLOT;   // 224 KiB
-// A gather thread infers from "its A slot is free" (the MMAs A_STAGES K-steps
-// back are done) that the W slot of the same K-step is free too (its last
-// user is W_STAGES K-steps back); that holds only with at least as many W
-// slots as A slots. Fewer would let the third A tile and the gather's
-// arrivals reach a W slot whose previous phase is still in use.
-static_assert(W_STAGES >= A_STAGES, "the A ring may not run further ahead than the W ring");
+// K-step j uses full/empty barrier pair j mod NBAR. Each producer waits for
+// the K-step its slot's previous user ran (j - W_STAGES for a W slot and for
+// m-tile 2 of a 3-m-tile unit, which lives in the W slot's second half;
+// j - A_STAGES for an A slot) before it arrives for K-step j. With more
+// barrier pairs than either lag, the phase a producer waits for can never be
+// overtaken by the next phase of the same barrier, and no arrival can reach
+// a barrier whose previous phase is still open.
+constexpr int NBAR = 8;
+static_assert(NBAR > W_STAGES && NBAR > A_STAGES, "barrier ring shorter than a slot lag");
 constexpr int UMMA_K = 16;
 constexpr uint32_t TMEM_COLS = 512;
 
 constexpr int EPI_WARPS = 4;                 // warps 0..3
 constexpr int MMA_WARP = 4;
 constexpr int W_WARP = 5;
-constexpr int GATHER_WARPS = 4;              // warps 6, 7, 9, 10 (warp 8 idles)
+constexpr int GATHER_WARPS = 4;              // warps 6, 7, 9, 10: m-tiles 0 and 1
 constexpr int GATHER_THREADS = GATHER_WARPS * 32;
-constexpr int THREADS = 11 * 32;
+constexpr int GATHER2_WARP = 11;             // m-tile 2 of 3-m-tile units
+constexpr int THREADS = 12 * 32;
 
 // Gather-thread index 0..127 of a thread in warps 6, 7, 9, 10; -1 otherwise.
 __device__ __forceinline__ int gather_index(int warp, int lane) {
@@ -123,14 +132,15 @@ __device__ __forceinline__ int gather_index(int warp, int lane) {
 constexpr int ROWS_PER_PASS = GATHER_THREADS / 8;    // 8 threads per 128-byte row segment
 constexpr int ROWS_PER_THREAD = BM / ROWS_PER_PASS;  // per m-tile
 constexpr int MAX_MPU = 3;                   // m-tiles per unit
+constexpr int ROWS2_PER_THREAD = BM / 4;     // warp 11: 4 rows per pass
 constexpr int SCHED_WARP = 8;
 constexpr int NQ = 8;                        // unit queue depth
 constexpr int QWORDS = 8;                    // e, row0, rows, mpu, n0, bn, bn_max, shared_w
 struct Ctrl {
     // One pair of barriers per K-step covers both rings: the K-step's W slot
     // and A slot fill up together and are freed by the same commit.
-    uint64_t wfull[W_STAGES];   // W producer arrive + tx bytes (+ one arrival per gather thread)
-    uint64_t wempty[W_STAGES];  // one tcgen05.commit
+    uint64_t wfull[NBAR];       // W producer arrive + tx bytes (+ one arrival per gather thread)
+    uint64_t wempty[NBAR];      // one tcgen05.commit
     uint64_t acc_full;          // one tcgen05.commit per unit
     uint64_t acc_empty;         // one arrive per epilogue warp
     uint64_t drain;
@@ -157,13 +167,14 @@ struct Cursor {
     }
 };
 
-// Cursor over the W ring that trails the current K-step by A_STAGES: slot
-// (j - A_STAGES) mod W_STAGES and the parity of that K-step's phase. Its
-// first A_STAGES positions name phase -1 (parity 1), which a fresh barrier
-// reports complete, so the first fills of the A ring do not wait.
-__device__ __forceinline__ Cursor<W_STAGES> lag_cursor() {
-    Cursor<W_STAGES> c;
-    c.s = (W_STAGES - A_STAGES) % W_STAGES;
+// Cursor over the barrier ring that trails the current K-step by L: entry
+// (j - L) mod NBAR and the parity of that K-step's phase. Its first L
+// positions name phase -1 (parity 1), which a fresh barrier reports
+// complete, so the first fills of a ring do not wait.
+template <int L>
+__device__ __forceinline__ Cursor<NBAR> lag_cursor() {
+    Cursor<NBAR> c;
+    c.s = (NBAR - L) % NBAR;
     c.ph = 1u;
     return c;
 }
@@ -307,8 +318,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     volatile int* abort = &ctl->abort;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < W_STAGES; ++s) {
-            mbar_init(wfull0 + 8 * s, kGather ? 1 + GATHER_THREADS : 1);
+        for (int s = 0; s < NBAR; ++s) {
+            mbar_init(wfull0 + 8 * s, kGather ? 1 + GATHER_THREADS + 32 : 1);
             mbar_init(wempty0 + 8 * s, 1);
         }
         mbar_init(acc_full, 1);
@@ -316,7 +327,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         mbar_init(drain, 1);
         for (int s = 0; s < NQ; ++s) {
             mbar_init(qfull0 + 8 * s, 1);
-            mbar_init(qempty0 + 8 * s, (kGather ? GATHER_WARPS : 0) + 2 + EPI_WARPS);
+            mbar_init(qempty0 + 8 * s, (kGather ? GATHER_WARPS + 1 : 0) + 2 + EPI_WARPS);
         }
         ctl->abort = 0;
         fence_barrier_init();
@@ -338,15 +349,15 @@ __global__ void __launch_bounds__(THREADS, 1)
     // 10 fall through to the final barrier.
     const int gt = gather_index(warp, lane);
     if (kGather && gt >= 0) {
-        // ------------------------------------------------------ dispatch
+        // ---------------------------------------- dispatch, m-tiles 0 and 1
         const int c = gt & 7;          // 16-byte chunk of the 128-byte row segment
         const int rb = gt >> 3;        // first row of this thread (0..15)
         const uint32_t swz = static_cast<uint32_t>(((c ^ (rb & 7)) << 4));
         const uint64_t pol_x = policy_evict_last();  // rows are re-read by the unit's other n-tiles
         Cursor<NQ> qc;
-        Cursor<W_STAGES> wc;
+        Cursor<NBAR> bc;
         Cursor<A_STAGES> ac;
-        Cursor<W_STAGES> back = lag_cursor();  // the K-step A_STAGES back
+        Cursor<NBAR> back = lag_cursor<A_STAGES>();  // the A slot's previous user
         bool ok = true, bad = false;
         while (ok) {
             Unit U;
@@ -355,9 +366,9 @@ __global__ void __launch_bounds__(THREADS, 1)
                 if (got < 0 && lane == 0) fail(abort, status);
                 break;
             }
-            const char* src[MAX_MPU][ROWS_PER_THREAD];
+            const char* src[2][ROWS_PER_THREAD];
 #pragma unroll
-            for (int mt = 0; mt < MAX_MPU; ++mt)
+            for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
                 for (int i = 0; i < ROWS_PER_THREAD; ++i) {
                     const int r = mt * BM + rb + ROWS_PER_PASS * i;
@@ -374,9 +385,6 @@ __global__ void __launch_bounds__(THREADS, 1)
                     src[mt][i] = p;
                 }
             for (int ks = 0; ks < nk; ++ks) {
-                // A slot free means the MMAs of the K-step three back are
-                // done, and with them those of the K-step four back, the last
-                // user of this K-step's W slot (its second half may take m-tile 2).
                 if (!warp_wait(wempty0 + 8 * back.s, back.ph, abort, limit)) {
                     if (lane == 0) fail(abort, status);
                     ok = false;
@@ -385,21 +393,88 @@ __global__ void __launch_bounds__(THREADS, 1)
                 const uint32_t nbytes = (ks * BKE + c * KCHUNK < D) ? 16u : 0u;
                 const int64_t koff = static_cast<int64_t>(ks) * ROW_BYTES;
 #pragma unroll
-                for (int mt = 0; mt < MAX_MPU; ++mt) {
-                    const uint32_t dst0 = a_tile(wc.s, ac.s, mt) + rb * 128 + swz;
+                for (int mt = 0; mt < 2; ++mt) {
+                    const uint32_t dst0 = sbase + A_RING_OFF + ac.s * A_SLOT + mt * A_BYTES + rb * 128 + swz;
 #pragma unroll
                     for (int i = 0; i < ROWS_PER_THREAD; ++i)
                         if (src[mt][i])
                             cp_async_16(dst0 + i * (ROWS_PER_PASS * 128),
                                         nbytes ? src[mt][i] + koff : src[mt][i], nbytes, pol_x);
                 }
-                cp_async_arrive_noinc(wfull0 + 8 * wc.s);
+                cp_async_arrive_noinc(wfull0 + 8 * bc.s);
+                bc.next();
                 ac.next();
-                wc.next();
                 back.next();
             }
         }
         // Copies still in flight must land before the CTA may exit.
+        cp_async_wait_all();
+        if (bad) report(status, PK_ERR_BAD_INDEX);
+    } else if (kGather && warp == GATHER2_WARP) {
+        // -------------------------- dispatch, m-tile 2 of 3-m-tile units
+        // Its own warp, so that its shorter lead (it writes the W slot's
+        // second half, whose previous user is W_STAGES K-steps back) does not
+        // hold back the arrivals of m-tiles 0 and 1, which a thread's
+        // cp.async arrivals would otherwise cover together. Every K-step it
+        // waits and arrives, also without rows to copy.
+        const int c = lane & 7;
+        const int rb = lane >> 3;      // rows rb + 4 i
+        const uint64_t pol_x = policy_evict_last();
+        Cursor<NQ> qc;
+        Cursor<NBAR> bc;
+        Cursor<W_STAGES> wc;
+        Cursor<NBAR> back = lag_cursor<W_STAGES>();  // the W slot's previous user
+        bool ok = true, bad = false;
+        while (ok) {
+            Unit U;
+            const int got = q_pop<true>(qfull0, qempty0, ctl->q, qc, U, abort, limit);
+            if (got <= 0) {
+                if (got < 0 && lane == 0) fail(abort, status);
+                break;
+            }
+            const int rows2 = U.mpu == 3 ? U.rows - 2 * BM : 0;  // valid rows of m-tile 2
+            int tok[ROWS2_PER_THREAD];                            // element offset of each row's x
+#pragma unroll
+            for (int i = 0; i < ROWS2_PER_THREAD; ++i) {
+                const int r = rb + 4 * i;
+                int off = -1;
+                if (r < rows2) {
+                    int f = __ldg(perm + U.row0 + 2 * BM + r);
+                    if (f < 0 || f >= R) {
+                        bad = true;
+                        f = 0;
+                    }
+                    off = f / k;
+                }
+                tok[i] = off;
+            }
+            for (int ks = 0; ks < nk; ++ks) {
+                if (!warp_wait(wempty0 + 8 * back.s, back.ph, abort, limit)) {
+                    if (lane == 0) fail(abort, status);
+                    ok = false;
+                    break;
+                }
+                if (rows2 > 0) {
+                    const uint32_t nbytes = (ks * BKE + c * KCHUNK < D) ? 16u : 0u;
+                    const int64_t koff = static_cast<int64_t>(ks) * ROW_BYTES;
+                    const uint32_t dst0 = sbase + wc.s * W_SLOT + (W_SLOT - A_BYTES);
+#pragma unroll
+                    for (int i = 0; i < ROWS2_PER_THREAD; ++i) {
+                        const int r = rb + 4 * i;
+                        if (tok[i] >= 0) {
+                            const char* p = reinterpret_cast<const char*>(
+                                                x + static_cast<int64_t>(tok[i]) * D * ELEM) + c * 16;
+                            cp_async_16(dst0 + r * 128 + static_cast<uint32_t>((c ^ (r & 7)) << 4),
+                                        nbytes ? p + koff : p, nbytes, pol_x);
+                        }
+                    }
+                }
+                cp_async_arrive_noinc(wfull0 + 8 * bc.s);
+                bc.next();
+                wc.next();
+                back.next();
+            }
+        }
         cp_async_wait_all();
         if (bad) report(status, PK_ERR_BAD_INDEX);
     } else if (warp == W_WARP) {
@@ -408,9 +483,12 @@ __global__ void __launch_bounds__(THREADS, 1)
             const uint64_t pol_once = policy_evict_first();
             const uint64_t pol_reuse = policy_evict_last();  // also A: re-read by every n-tile
             Cursor<NQ> qc;
+            Cursor<NBAR> bc;
             Cursor<W_STAGES> wc;
             Cursor<A_STAGES> ac;
-            Cursor<W_STAGES> back = lag_cursor();
+            // the W slot's previous user (grouped GEMM: also m-tile 2's slot; the
+            // A slot's previous user is one K-step older still)
+            Cursor<NBAR> back = lag_cursor<W_STAGES>();
             uint32_t w_issued = 0, w_par = 0;
             bool ok = true;
             // Failure-detection test hook (off: stall < 0): CTA stall >> 40 arms
@@ -434,15 +512,12 @@ __global__ void __launch_bounds__(THREADS, 1)
                                      (!kGather && U.mpu > 2 ? static_cast<uint32_t>(A_BYTES) : 0u);
                 const uint32_t atx = static_cast<uint32_t>(a_lo * A_BYTES);
                 for (int ks = 0; ks < nk; ++ks) {
-                    // W slot: free once the K-step W_STAGES back is done; grouped
-                    // GEMM (A by TMA as well): once the one A_STAGES back is done.
-                    if (!(kGather ? mbar_wait(wempty0 + 8 * wc.s, wc.ph ^ 1u, abort, limit)
-                                  : mbar_wait(wempty0 + 8 * back.s, back.ph, abort, limit))) {
+                    if (!mbar_wait(wempty0 + 8 * back.s, back.ph, abort, limit)) {
                         fail(abort, status);
                         ok = false;
                         break;
                     }
-                    const uint32_t wfull = wfull0 + 8 * wc.s;
+                    const uint32_t wfull = wfull0 + 8 * bc.s;
                     mbar_arrive_expect_tx(wfull, kGather ? wtx : wtx + atx);
                     const uint32_t wsl = sbase + wc.s * W_SLOT;
                     const bool stalled = kcount++ == stall_step;
@@ -457,21 +532,22 @@ __global__ void __launch_bounds__(THREADS, 1)
                                         U.e, wfull, pol);
                     }
                     if (!stalled) {
-                        w_issued |= 1u << wc.s;
-                        w_par = (w_par & ~(1u << wc.s)) | (wc.ph << wc.s);
+                        w_issued |= 1u << bc.s;
+                        w_par = (w_par & ~(1u << bc.s)) | (bc.ph << bc.s);
                     }
                     if (!kGather && !stalled) {  // rows past the expert's end are loaded but never stored
                         for (int mt = 0; mt < U.mpu; ++mt)
                             tma_load_2d(a_tile(wc.s, ac.s, mt), &amap, ks * BKE, U.row0 + mt * BM,
                                         wfull, pol_reuse);
                     }
+                    bc.next();
                     wc.next();
                     ac.next();
                     back.next();
                 }
             }
             // Every copy this thread started must land before the CTA may exit.
-            for (int s = 0; s < W_STAGES; ++s)
+            for (int s = 0; s < NBAR; ++s)
                 if ((w_issued >> s) & 1u) mbar_wait(wfull0 + 8 * s, (w_par >> s) & 1u, nullptr, limit);
         }
         __syncwarp();
@@ -479,6 +555,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         // ----------------------------------------------------------- MMA
         if (lane == 0) {
             Cursor<NQ> qc;
+            Cursor<NBAR> bc;
             Cursor<W_STAGES> wc;
             Cursor<A_STAGES> ac;
             uint32_t acc_phase = 0;
@@ -511,7 +588,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 const int mpu = U.mpu;
                 const uint32_t acc_stride = static_cast<uint32_t>(U.bn_max);
                 for (int ks = 0; ks < nk; ++ks) {
-                    if (!mbar_wait(wfull0 + 8 * wc.s, wc.ph, abort, limit)) {
+                    if (!mbar_wait(wfull0 + 8 * bc.s, bc.ph, abort, limit)) {
                         fail(abort, status);
                         ok = false;
                         break;
@@ -534,7 +611,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                                          (ks | kk) != 0 ? 1u : 0u);
                         }
                     }
-                    mma_commit(wempty0 + 8 * wc.s);
+                    mma_commit(wempty0 + 8 * bc.s);
+                    bc.next();
                     wc.next();
                     ac.next();
                 }
