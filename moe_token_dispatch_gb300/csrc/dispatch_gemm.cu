@@ -267,6 +267,54 @@ __device__ __forceinline__ void store_row_chunk(uint16_t* dst, const uint32_t (&
     }
 }
 
+// 64 accumulator columns of the warp's 32 rows (lane = row; v0 holds columns
+// col0 .. col0+31, v1 the next 32) -> bf16, then a 4 x 4 transpose of 32-byte
+// blocks inside each group of four lanes, so that lane 4g + c holds block c
+// (16 columns) of rows 4g .. 4g+3 and each of the four store instructions
+// writes eight rows x 128 contiguous bytes (instead of 32 rows x 32 bytes).
+// Every lane of the warp must call this; rows >= nrows and columns >= De are
+// not stored. Needs De % 16 == 0 and a 32-byte aligned out.
+__device__ __forceinline__ void store_rows_quad(uint16_t* out, int64_t row0, int nrows, int De,
+                                                const uint32_t (&v0)[32], const uint32_t (&v1)[32],
+                                                int col0) {
+    const int lane = static_cast<int>(threadIdx.x & 31);
+    const int c = lane & 3;
+    uint32_t b0[8], b1[8], b2[8], b3[8];  // 16-column blocks 0..3 of this lane's row
+#pragma unroll
+    for (int w = 0; w < 8; ++w) {
+        b0[w] = pack_bf16x2(v0[2 * w], v0[2 * w + 1]);
+        b1[w] = pack_bf16x2(v0[16 + 2 * w], v0[16 + 2 * w + 1]);
+        b2[w] = pack_bf16x2(v1[2 * w], v1[2 * w + 1]);
+        b3[w] = pack_bf16x2(v1[16 + 2 * w], v1[16 + 2 * w + 1]);
+    }
+    const bool odd = (c & 1) != 0, hi = (c & 2) != 0;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) {
+        // lanes 2a, 2a+1 swap across blocks (0,1) and (2,3)
+        uint32_t r = __shfl_xor_sync(0xffffffffu, odd ? b0[w] : b1[w], 1);
+        if (odd) b0[w] = r; else b1[w] = r;
+        r = __shfl_xor_sync(0xffffffffu, odd ? b2[w] : b3[w], 1);
+        if (odd) b2[w] = r; else b3[w] = r;
+        // lanes a, a+2 swap across block pairs (0,1) and (2,3)
+        r = __shfl_xor_sync(0xffffffffu, hi ? b0[w] : b2[w], 2);
+        if (hi) b0[w] = r; else b2[w] = r;
+        r = __shfl_xor_sync(0xffffffffu, hi ? b1[w] : b3[w], 2);
+        if (hi) b1[w] = r; else b3[w] = r;
+    }
+    const int col = col0 + 16 * c;
+    if (col >= De) return;
+    const int rq = lane & ~3;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        if (rq + i >= nrows) break;
+        const uint32_t* s = i == 0 ? b0 : i == 1 ? b1 : i == 2 ? b2 : b3;
+        uint16_t* dst = out + (row0 + rq + i) * static_cast<int64_t>(De) + col;
+        asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(dst), "r"(s[0]),
+                     "r"(s[1]), "r"(s[2]), "r"(s[3]), "r"(s[4]), "r"(s[5]), "r"(s[6]), "r"(s[7])
+                     : "memory");
+    }
+}
+
 // FP8 epilogue: accumulator x row scale, then x column scale (fp32). Lane L
 // holds the scale of column col0 + L (`cs`); column j's is broadcast to the
 // whole warp by a shuffle, so every lane of the warp must call this.
@@ -707,9 +755,12 @@ __global__ void __launch_bounds__(THREADS, 1)
                         scale_chunk(v0, rs, cs0);
                         scale_chunk(v1, rs, cs1);
                     }
-                    if (valid) {
-                        store_row_chunk(orow, v0, U.n0 + cc * 32, De, wide);
-                        store_row_chunk(orow, v1, U.n0 + cc * 32 + 32, De, wide);
+                    if (wide) {
+                        store_rows_quad(out, static_cast<int64_t>(U.row0) + rbase, U.rows - rbase, De,
+                                        v0, v1, U.n0 + cc * 32);
+                    } else if (valid) {
+                        store_row_chunk(orow, v0, U.n0 + cc * 32, De, false);
+                        store_row_chunk(orow, v1, U.n0 + cc * 32 + 32, De, false);
                     }
                 }
             }
