@@ -55,7 +55,8 @@ typedef enum {
     PK_ERR_UNSUPPORTED = 2,
     PK_ERR_CUDA = 3,
     PK_ERR_TIMEOUT = 4,
-    PK_ERR_BAD_INDEX = 5
+    PK_ERR_BAD_INDEX = 5,
+    PK_ERR_CAPTURE = 6
 } pk_status;
 
 /* Largest number of experts the routing kernels accept. */
@@ -66,8 +67,9 @@ const char* pk_status_str(int status);
 
 /* Version of this ABI (major * 10000 + minor * 100 + patch). 1.1: FP8
  * entry points (quantisation, dispatch and grouped GEMM), GEMM kernel
- * selection, routing launch count. */
-#define PK_ABI_VERSION 10100
+ * selection, routing launch count. 1.2: PK_ERR_CAPTURE, the GEMM stall test
+ * hook. */
+#define PK_ABI_VERSION 10200
 int pk_abi_version(void);
 
 /*
@@ -189,8 +191,10 @@ int pk_moe_quant_rows(const uint16_t* x, int32_t T, int32_t D, uint8_t* xq, floa
  *   wq[(((e * NB + n / 64) * KB + d / 128) * 64 + n % 64) * 128 + d % 128]
  *     = code(e, n, d),  NB = ceil(N / 64), KB = ceil(D / 128),
  * and every byte of a block past N or D is 0.
- *   W   device bf16 [E, D, N]; wq device uint8, pk_moe_fp8_weight_bytes(E, D, N)
- *   bytes; sw device fp32 [E, N].
+ *   W   device bf16 [E, D, N], 16-byte aligned; wq device uint8,
+ *   pk_moe_fp8_weight_bytes(E, D, N) bytes, 16-byte aligned; sw device fp32
+ *   [E, N], 4-byte aligned. A misaligned pointer returns PK_ERR_INVALID_ARG
+ *   before any CUDA call.
  */
 size_t pk_moe_fp8_weight_bytes(int32_t E, int32_t D, int32_t N);
 int pk_moe_quant_weights(const uint16_t* W, int32_t E, int32_t D, int32_t N, uint8_t* wq,
@@ -274,8 +278,11 @@ int pk_moe_combine(const uint16_t* src, const int32_t* inv_perm, const float* ga
  * until the process exits. Sizes with ceil(T*k / 2048) * E * 4 bytes above
  * that limit are rejected with PK_ERR_UNSUPPORTED (E = 256 allows T*k up to
  * 2,097,152). The call allocates nothing and calls no cudaMalloc/cudaFree.
- *   The first call on each device looks up the array's device address with
- * that device current; make that first call before any stream capture. Every
+ *   The array's device address is looked up with the device current on the
+ * first call in each CUDA context (and again when the current context is a
+ * new one, e.g. after cudaDeviceReset), never during stream capture: a first
+ * call in a context that is made while `stream` is being captured returns
+ * PK_ERR_CAPTURE and launches nothing -- make one call before capturing. Every
  * call shares the one array and leaves its contents behind; each call rewrites
  * every counter it reads, so nothing needs clearing, but calls that overlap on
  * the GPU (other streams or host threads) race: order them on one stream.

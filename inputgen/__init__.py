@@ -171,6 +171,12 @@ WORKLOADS = {
     # "decode", 32 experts so that W (0.94 GB) still exceeds L2
     "decode32": Workload("decode32", 16, 7168, 32, 8, 2048,
                          desc="decode shape with 32 experts and 16 tokens (profiling size)"),
+    # profiling case for the skewed workload: the Zipf-biased routing of "skew"
+    # over 32 experts and 1024 tokens, so one expert holds most tokens (a
+    # heavy expert of several row groups next to light and empty ones) while
+    # W (0.94 GB) still exceeds L2
+    "skew32": Workload("skew32", 1024, 7168, 32, 8, 2048, zipf_s=1.2,
+                       desc="skewed routing over 32 experts and 1024 tokens (profiling size)"),
 }
 
 

@@ -10,6 +10,7 @@ and streams only.
 from ._binding import (  # noqa: F401
     LIB_PATH,
     PK_ERR_BAD_INDEX,
+    PK_ERR_CAPTURE,
     PK_ERR_CUDA,
     PK_ERR_INVALID_ARG,
     PK_ERR_TIMEOUT,

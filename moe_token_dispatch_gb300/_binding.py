@@ -20,6 +20,7 @@ PK_ERR_UNSUPPORTED = 2
 PK_ERR_CUDA = 3
 PK_ERR_TIMEOUT = 4
 PK_ERR_BAD_INDEX = 5
+PK_ERR_CAPTURE = 6
 PK_MAX_EXPERTS = 4096
 PK_NOALLOC_SCRATCH_BYTES = 1 << 20
 PK_ROUTER_MAX_EXPERTS = 1024
@@ -282,8 +283,9 @@ def pk_moe_route_noalloc(topk_idx: torch.Tensor, E: int, expert_offsets: torch.T
     """Counts, offsets, perm and inv_perm without a caller workspace: for
     callers that cannot allocate device memory (the C call allocates none;
     its counters live in a fixed 1 MiB array inside the library). The first
-    call on a device should come before any stream capture; calls that
-    overlap on the GPU share that array and race."""
+    call in a CUDA context must come before any stream capture (made during
+    capture it raises PkError with PK_ERR_CAPTURE); calls that overlap on the
+    GPU share that array and race."""
     T, k = topk_idx.shape
     rc = lib.pk_moe_route_noalloc(
         _ptr(topk_idx, torch.int32, "topk_idx"), T, k, E,

@@ -34,6 +34,7 @@ const char* pk_status_str(int status) {
         case PK_ERR_CUDA: return "PK_ERR_CUDA";
         case PK_ERR_TIMEOUT: return "PK_ERR_TIMEOUT";
         case PK_ERR_BAD_INDEX: return "PK_ERR_BAD_INDEX";
+        case PK_ERR_CAPTURE: return "PK_ERR_CAPTURE";
         default: return "PK_ERR_UNKNOWN";
     }
 }
@@ -144,6 +145,9 @@ int pk_moe_quant_weights(const uint16_t* W, int32_t E, int32_t D, int32_t N, uin
     if (E < 1 || D < 1 || N < 1) return PK_ERR_INVALID_ARG;
     if (E > 65535) return PK_ERR_UNSUPPORTED;  // experts are a grid dimension
     if (!W || !wq || !sw) return PK_ERR_INVALID_ARG;
+    // the GEMMs read W and wq by TMA (16-byte aligned) and sw as fp32
+    if (!aligned16(W) || !aligned16(wq) || (reinterpret_cast<uintptr_t>(sw) & 3u) != 0)
+        return PK_ERR_INVALID_ARG;
     cudaError_t err =
         pk::launch_quant_cols(W, E, D, N, wq, sw, static_cast<cudaStream_t>(stream));
     return err == cudaSuccess ? PK_OK : PK_ERR_CUDA;

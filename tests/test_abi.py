@@ -129,6 +129,10 @@ def test_quant_entry_points_reject(lib):
     assert L.pk_moe_quant_rows(None, 0, 16, None, None, None) == 0        # T == 0: no-op
     assert L.pk_moe_quant_weights(FAKE, 0, 16, 16, FAKE, FAKE, None) == 1
     assert L.pk_moe_quant_weights(FAKE, 70000, 16, 16, FAKE, FAKE, None) == 2
+    # W and wq 16-byte aligned, sw 4-byte aligned, checked before any CUDA call
+    assert L.pk_moe_quant_weights(FAKE_ODD, 2, 16, 16, FAKE, FAKE, None) == 1
+    assert L.pk_moe_quant_weights(FAKE, 2, 16, 16, FAKE_ODD, FAKE, None) == 1
+    assert L.pk_moe_quant_weights(FAKE, 2, 16, 16, FAKE, ctypes.c_void_p(0x10002), None) == 1
     assert L.pk_moe_dispatch_gemm_fp8(None, None, None, None, None, None, 0, 2, 64, 8, 64,
                                       None, None, None) == 0
 
@@ -166,3 +170,24 @@ def test_grouped_gemm_fp8_rejects(lib):
     assert L.pk_moe_grouped_gemm_fp8(FAKE, FAKE, FAKE, FAKE, FAKE, 8, 64, 12, 2, FAKE, None, None) == 1
     assert L.pk_moe_grouped_gemm_fp8(FAKE, None, FAKE, FAKE, FAKE, 8, 64, 64, 2, FAKE, None, None) == 1
     assert L.pk_moe_grouped_gemm_fp8(None, None, None, None, None, 0, 64, 64, 2, None, None, None) == 0
+
+
+def _code_only(path):
+    """C/C++ source without comments or string literals."""
+    import re
+    text = open(path).read()
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return re.sub(r'"(?:\\.|[^"\\])*"', '""', text)
+
+
+def test_noalloc_path_names_no_allocation_call():
+    """The allocation-free routing entry point and the routing launch helpers
+    it calls contain no device or host allocation call (comments aside)."""
+    import re
+    csrc = os.path.join(ROOT, "moe_token_dispatch_gb300", "csrc")
+    pat = re.compile(r"\b(cudaMalloc\w*|cudaFree\w*|cuMemAlloc\w*|cuMemFree\w*|cuMemCreate|"
+                     r"cudaHostAlloc|cudaMallocHost|malloc|calloc|realloc|new)\s*[\(\[]")
+    for name in ("route_noalloc.cu", "route.cu"):
+        hits = pat.findall(_code_only(os.path.join(csrc, name)))
+        assert not hits, (name, hits)
