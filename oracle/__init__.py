@@ -83,6 +83,14 @@ def _L():
         lib.oracle_quant_cols.restype = None
         lib.oracle_quant_cols.argtypes = [_P, _I, _I, _I, _P, _P]
         lib.oracle_gemm_fp8_rows.restype = ctypes.c_int
+        lib.oracle_e8m0_to_f64.restype = ctypes.c_double
+        lib.oracle_e8m0_to_f64.argtypes = [ctypes.c_uint8]
+        lib.oracle_mx_quant_rows.restype = ctypes.c_int
+        lib.oracle_mx_quant_rows.argtypes = [_P, _I, _I, _P, _P]
+        lib.oracle_mx_quant_cols.restype = ctypes.c_int
+        lib.oracle_mx_quant_cols.argtypes = [_P, _I, _I, _I, _P, _P]
+        lib.oracle_gemm_mx_rows.restype = ctypes.c_int
+        lib.oracle_gemm_mx_rows.argtypes = [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _I, _P]
         lib.oracle_gemm_fp8_rows.argtypes = [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _I,
                                              _P]
         lib.oracle_gemm_rows.restype = ctypes.c_int
@@ -239,6 +247,56 @@ def gemm_fp8_rows(xq, sx, perm, offsets, wq, sw, k, rows) -> np.ndarray:
                                                T, k, D, E, N, rows.ctypes.data, rows.size,
                                                out.ctypes.data):
         raise OracleError("row outside every expert segment, or token out of range")
+    return out
+
+
+def e8m0_to_f64(b: int) -> float:
+    return float(_L().oracle_e8m0_to_f64(b))
+
+
+def mx_quant_rows(x: np.ndarray):
+    """MXFP8 of the rows of bf16 x [T, D] (D a multiple of 32): E4M3 codes
+    [T, D] and E8M0 scale bytes [T, D // 32] (one per 32 consecutive d)."""
+    x = _c(x, np.uint16)
+    T, D = x.shape
+    q = np.zeros((T, D), dtype=np.uint8)
+    s = np.zeros((T, D // 32), dtype=np.uint8)
+    if T and _L().oracle_mx_quant_rows(x.ctypes.data, T, D, q.ctypes.data, s.ctypes.data):
+        raise OracleError("D must be a multiple of 32")
+    return q, s
+
+
+def mx_quant_cols(W: np.ndarray):
+    """MXFP8 of the columns of bf16 W [E, D, N] (blocks of 32 along d): codes
+    [E, N, D] (each output column contiguous) and E8M0 bytes [E, N, D // 32]."""
+    W = np.asarray(W)
+    assert W.dtype == np.uint16 and W.flags.c_contiguous
+    E, D, N = W.shape
+    q = np.zeros((E, N, D), dtype=np.uint8)
+    s = np.zeros((E, N, D // 32), dtype=np.uint8)
+    if _L().oracle_mx_quant_cols(W.ctypes.data, E, D, N, q.ctypes.data, s.ctypes.data):
+        raise OracleError("D must be a multiple of 32")
+    return q, s
+
+
+def gemm_mx_rows(xq, sx, perm, offsets, wq, sw, k, rows) -> np.ndarray:
+    """float64 [len(rows), N] of the MXFP8 expert GEMM from codes and E8M0
+    block scales (mx_quant_rows of x, mx_quant_cols of W)."""
+    xq, sx = _c(xq, np.uint8), _c(sx, np.uint8)
+    wq, sw = np.asarray(wq), np.asarray(sw)
+    assert wq.dtype == np.uint8 and wq.flags.c_contiguous
+    assert sw.dtype == np.uint8 and sw.flags.c_contiguous
+    T, D = xq.shape
+    E, N, D2 = wq.shape
+    assert D2 == D and sx.shape == (T, D // 32) and sw.shape == (E, N, D // 32)
+    perm, offsets = _c(perm, np.int64), _c(offsets, np.int64)
+    rows = _c(np.asarray(rows).reshape(-1), np.int64)
+    out = np.zeros((rows.size, N), dtype=np.float64)
+    if rows.size and _L().oracle_gemm_mx_rows(xq.ctypes.data, sx.ctypes.data, perm.ctypes.data,
+                                              offsets.ctypes.data, wq.ctypes.data, sw.ctypes.data,
+                                              T, k, D, E, N, rows.ctypes.data, rows.size,
+                                              out.ctypes.data):
+        raise OracleError("row outside every expert segment, token out of range or D % 32")
     return out
 
 

@@ -293,3 +293,106 @@ int oracle_gemm_fp8_rows(const uint8_t* xq, const float* sx, const int64_t* perm
     }
     return 0;
 }
+
+/* ---------------------------------------------------------------------- */
+/* Microscaling FP8 (MXFP8), the block-scaled FP8 form that the tutorial
+ * page's "ThunderKittens 2.0 & FP8/NVFP4" item names. The pages do not
+ * define it; this follows the definition of the MX formats (OCP Microscaling
+ * Formats specification): 32 consecutive elements along the reduction
+ * dimension share one scale X = 2^s, stored as an 8-bit power of two (E8M0:
+ * the byte s + 127), and each element is the E4M3 code of v / X. One block:
+ *   amax = max |v_i|;
+ *   s    = floor(log2(amax)) - 8, clamped to [-127, 127] (8 is the exponent
+ *          of E4M3's largest normal value, 448 = 1.75 * 2^8), so that the
+ *          block's largest magnitude lands in [256, 512) before conversion;
+ *   code_i = E4M3(v_i / 2^s): round to nearest even, magnitudes above 448
+ *          saturated to 448 (only the block maximum can reach [448, 512));
+ *   an all-zero block takes s = -127 (byte 0) and zero codes.
+ * The dequantised element is value(code_i) * 2^s; v / 2^s is formed exactly
+ * (a power-of-two scaling of a bf16 value). */
+static int mx_shared_exp(double amax) {
+    if (amax == 0.0) return -127;
+    int e = (int)floor(log2(amax));
+    if (ldexp(1.0, e) > amax) e -= 1;      /* guard log2 rounding */
+    if (ldexp(1.0, e + 1) <= amax) e += 1;
+    int s = e - 8;
+    if (s < -127) s = -127;
+    if (s > 127) s = 127;
+    return s;
+}
+
+/* One block of n values `stride` apart -> n codes `qstride` apart; returns
+ * the E8M0 byte. */
+static uint8_t mx_block(const uint16_t* v, int64_t n, int64_t stride, uint8_t* q, int64_t qstride) {
+    double amax = 0.0;
+    for (int64_t i = 0; i < n; ++i) {
+        const double a = fabs(oracle_bf16_to_f64(v[i * stride]));
+        if (a > amax) amax = a;
+    }
+    const int s = mx_shared_exp(amax);
+    for (int64_t i = 0; i < n; ++i)
+        q[i * qstride] = oracle_f32_to_e4m3((float)ldexp(oracle_bf16_to_f64(v[i * stride]), -s));
+    return (uint8_t)(s + 127);
+}
+
+/* E8M0 byte -> its power of two (byte 255 is NaN in the format; unused here). */
+double oracle_e8m0_to_f64(uint8_t b) {
+    if (b == 255u) return NAN;
+    return ldexp(1.0, (int)b - 127);
+}
+
+/* Rows of x [T, D], D a multiple of 32: xq [T, D] codes, sx [T, D / 32]
+ * E8M0 bytes (block b of row t covers d in [32 b, 32 b + 32)). Returns 1 if
+ * D is not a multiple of 32. */
+int oracle_mx_quant_rows(const uint16_t* x, int64_t T, int64_t D, uint8_t* xq, uint8_t* sx) {
+    if (D % 32 != 0) return 1;
+    const int64_t nb = D / 32;
+    for (int64_t t = 0; t < T; ++t)
+        for (int64_t b = 0; b < nb; ++b)
+            sx[t * nb + b] = mx_block(x + t * D + 32 * b, 32, 1, xq + t * D + 32 * b, 1);
+    return 0;
+}
+
+/* Columns of every W[e] [D, N] (blocks along d): codes stored transposed,
+ * wq [E, N, D] (each output column's D codes contiguous), sw [E, N, D / 32].
+ * Returns 1 if D is not a multiple of 32. */
+int oracle_mx_quant_cols(const uint16_t* W, int64_t E, int64_t D, int64_t N, uint8_t* wq,
+                         uint8_t* sw) {
+    if (D % 32 != 0) return 1;
+    const int64_t nb = D / 32;
+    for (int64_t e = 0; e < E; ++e)
+        for (int64_t n = 0; n < N; ++n)
+            for (int64_t b = 0; b < nb; ++b)
+                sw[(e * N + n) * nb + b] = mx_block(W + (e * D + 32 * b) * N + n, 32, N,
+                                                    wq + (e * N + n) * D + 32 * b, 1);
+    return 0;
+}
+
+/* The MXFP8 expert GEMM for the listed sorted rows, float64:
+ *   out[j][n] = sum_d (value(xq[t][d]) * 2^(sx[t][d/32] - 127))
+ *                   * (value(wq[e][n][d]) * 2^(sw[e][n][d/32] - 127)),
+ * d ascending, t = perm[j] / k, e = e(j). */
+int oracle_gemm_mx_rows(const uint8_t* xq, const uint8_t* sx, const int64_t* perm,
+                        const int64_t* offsets, const uint8_t* wq, const uint8_t* sw, int64_t T,
+                        int64_t k, int64_t D, int64_t E, int64_t N, const int64_t* rows,
+                        int64_t nrows, double* out) {
+    if (D % 32 != 0) return 1;
+    const int64_t nb = D / 32;
+    for (int64_t r = 0; r < nrows; ++r) {
+        const int64_t j = rows[r];
+        const int64_t e = oracle_expert_of_row(offsets, E, j);
+        if (e < 0) return 1;
+        const int64_t t = perm[j] / k;
+        if (t < 0 || t >= T) return 1;
+        for (int64_t n = 0; n < N; ++n) {
+            const uint8_t* wcol = wq + (e * N + n) * D;
+            const uint8_t* wsc = sw + (e * N + n) * nb;
+            double acc = 0.0;
+            for (int64_t d = 0; d < D; ++d)
+                acc += (oracle_e4m3_to_f64(xq[t * D + d]) * oracle_e8m0_to_f64(sx[t * nb + d / 32])) *
+                       (oracle_e4m3_to_f64(wcol[d]) * oracle_e8m0_to_f64(wsc[d / 32]));
+            out[r * N + n] = acc;
+        }
+    }
+    return 0;
+}

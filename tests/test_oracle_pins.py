@@ -466,3 +466,156 @@ def test_planted_fp8_mistakes_are_caught():
         check_gemm_fp8(scale_swapped, np.random.default_rng(34))
     with pytest.raises(AssertionError):
         check_quant_rows(unscaled_rows, np.random.default_rng(32))
+
+
+# ------------------------------------------------------------ MXFP8 pins
+# The MX formats' definition (32-element blocks along the reduction axis,
+# one E8M0 power-of-two scale 2^s per block, s = floor(log2 amax) - 8 for
+# E4M3 elements, codes E4M3(v / 2^s) with saturation) worked by hand.
+def _bf16_vec(vals, n=32):
+    v = np.zeros(n, dtype=np.float32)
+    v[: len(vals)] = vals
+    return (v.view(np.uint32) >> 16).astype(np.uint16)
+
+
+MX_HAND_WORKED = [
+    # (block values, E8M0 byte, codes of the listed values)
+    ([448.0], 127, [0x7E]),                        # amax 448: s = 0, 448 itself
+    ([1.0, -0.5, 0.25], 119, [0x78, 0xF0, 0x68]),  # s = -8: 256, -128, 64
+    ([1.0, -0.5, 0.25, 3.0], 120, [0x70, 0xE8, 0x60, 0x7C]),  # s = -7: 128, -64, 32, 384
+    ([500.0, 1.0], 127, [0x7E, 0x38]),             # s = 0: 500 saturates to 448; 1.0 stays
+    ([], 0, []),                                   # all zero: byte 0, zero codes
+    ([2.0 ** -130], 0, [0x20]),                    # s clamps at -127: 2^-130 / 2^-127 = 2^-3
+    ([2.0 ** 127, 2.0 ** 118], 246, [0x78, 0x30]), # s = 119: 2^8 = 256 and 2^-1
+]
+
+
+def test_mx_hand_worked_blocks():
+    for vals, byte, codes in MX_HAND_WORKED:
+        x = _bf16_vec(vals)[None, :]
+        q, s = oracle.mx_quant_rows(x)
+        assert s[0, 0] == byte, (vals, s[0, 0])
+        assert [int(c) for c in q[0, : len(codes)]] == codes, (vals, [hex(c) for c in q[0]])
+        assert not q[0, len(codes):].any()
+    assert oracle.e8m0_to_f64(127) == 1.0 and oracle.e8m0_to_f64(0) == 2.0 ** -127
+    assert oracle.e8m0_to_f64(254) == 2.0 ** 127 and math.isnan(oracle.e8m0_to_f64(255))
+
+
+def check_mx_quant_rows(qr, rng):
+    x = bf16((rng.standard_normal((6, 128)) * np.exp(rng.uniform(-8, 8, (6, 4)).repeat(32, 1)))
+             .astype(np.float32))
+    x[2, 32:64] = 0                               # an all-zero block
+    q, s = qr(x)
+    assert q.shape == x.shape and s.shape == (6, 4) and s.dtype == np.uint8
+    xf = ig.bf16_bits_to_f64(x)
+    X = np.ldexp(1.0, s.astype(np.int64) - 127).repeat(32, 1)
+    deq = np.vectorize(oracle.e4m3_to_f64)(q) * X
+    scaled = np.abs(xf) / X
+    # each block's largest magnitude lands in [256, 512) before conversion
+    for t in range(6):
+        for b in range(4):
+            blk = scaled[t, 32 * b: 32 * b + 32]
+            if blk.max() == 0:
+                assert s[t, b] == 0 and not q[t, 32 * b: 32 * b + 32].any()
+            else:
+                assert 256.0 <= blk.max() < 512.0, (t, b, blk.max())
+    # reconstruction within E4M3's error (half a step of the 3-bit mantissa,
+    # half the subnormal step below 2^-6), except the values above 448 that
+    # saturate
+    sat = scaled > 448.0
+    err = np.abs(deq - xf)
+    ok = err <= 2.0 ** -4 * np.abs(xf) + 2.0 ** -10 * X
+    assert np.all(ok | sat)
+    assert np.all(np.abs(deq[sat]) == 448.0 * X[sat])
+    # without saturation the codes are torch's round-to-nearest-even E4M3 cast
+    import torch
+    v = torch.from_numpy((xf / X).astype(np.float32)[~sat])
+    assert np.array_equal(q[~sat], v.to(torch.float8_e4m3fn).view(torch.uint8).numpy())
+
+
+def test_mx_quant_rows_and_cols():
+    check_mx_quant_rows(oracle.mx_quant_rows, np.random.default_rng(41))
+    rng = np.random.default_rng(42)
+    W = bf16((rng.standard_normal((3, 96, 40)) / 10).astype(np.float32))
+    q, s = oracle.mx_quant_cols(W)
+    # blocks run along d: the columns of W[e] are the rows of W[e].T
+    for e in range(3):
+        qe, se = oracle.mx_quant_rows(np.ascontiguousarray(W[e].T))
+        assert np.array_equal(q[e], qe) and np.array_equal(s[e], se)
+    # a change inside one block changes that block's codes and scale only
+    x = bf16(rng.standard_normal((1, 96)).astype(np.float32))
+    q0, s0 = oracle.mx_quant_rows(x)
+    x2 = x.copy()
+    x2[0, 40] = (np.array([1e3], np.float32).view(np.uint32) >> 16).astype(np.uint16)[0]
+    q2, s2 = oracle.mx_quant_rows(x2)
+    assert s2[0, 1] != s0[0, 1] and s2[0, 0] == s0[0, 0] and s2[0, 2] == s0[0, 2]
+    assert np.array_equal(q2[0, :32], q0[0, :32]) and np.array_equal(q2[0, 64:], q0[0, 64:])
+    with pytest.raises(oracle.OracleError):
+        oracle.mx_quant_rows(bf16(np.zeros((1, 48), np.float32)))
+
+
+def check_gemm_mx(gemm, rng):
+    T, k, E, D, N = 19, 2, 4, 96, 40
+    topk = np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int32)
+    _, offsets = oracle.route_counts(topk, E)
+    perm, _ = oracle.build_perm(topk, E, offsets)
+    x = bf16((rng.standard_normal((T, D)) * np.exp(rng.uniform(-3, 3, (T, 3)).repeat(32, 1)))
+             .astype(np.float32))
+    W = bf16((rng.standard_normal((E, D, N)) / 8).astype(np.float32))
+    xq, sx = oracle.mx_quant_rows(x)
+    wq, sw = oracle.mx_quant_cols(W)
+    out = gemm(xq, sx, perm, offsets, wq, sw, k, np.arange(T * k))
+    deq = np.vectorize(oracle.e4m3_to_f64)
+    xd = deq(xq) * np.ldexp(1.0, sx.astype(np.int64) - 127).repeat(32, 1)
+    wd = deq(wq) * np.ldexp(1.0, sw.astype(np.int64) - 127).repeat(32, 2)   # [E, N, D]
+    for e in range(E):
+        lo, hi = offsets[e], offsets[e + 1]
+        ref = xd[perm[lo:hi] // k] @ wd[e].T
+        assert np.all(np.abs(out[lo:hi] - ref) <= 1e-12 * (np.abs(xd[perm[lo:hi] // k]) @ np.abs(wd[e]).T))
+    # one element by brute force with exact summation
+    j, n = 5, 7
+    e = int(np.searchsorted(offsets, j, side="right") - 1)
+    t = perm[j] // k
+    assert math.isclose(out[j, n], math.fsum(xd[t] * wd[e, n]), rel_tol=1e-12, abs_tol=1e-300)
+    # and it approximates the bf16 GEMM within E4M3's precision
+    bf = oracle.gemm_rows(x, perm, offsets, W, k, np.arange(T * k))
+    assert np.abs(out - bf).max() < 0.1 * np.abs(bf).max()
+
+
+def test_gemm_mx_pins():
+    check_gemm_mx(oracle.gemm_mx_rows, np.random.default_rng(43))
+
+
+def test_planted_mx_mistakes_are_caught():
+    def emax7(x):                         # s = floor(log2 amax) - 7: the block max lands in [128, 256)
+        q, s = oracle.mx_quant_rows(x)
+        xf = ig.bf16_bits_to_f64(x)
+        s = np.where(s > 0, s + 1, s).astype(np.uint8)
+        X = np.ldexp(1.0, s.astype(np.int64) - 127).repeat(32, 1)
+        q = np.array([[oracle.f32_to_e4m3(float(v)) for v in row] for row in xf / X], np.uint8)
+        return q, s
+
+    def ceil_exp(x):                      # ceil instead of floor: only exact powers of two agree
+        q, s = oracle.mx_quant_rows(x)
+        xf = ig.bf16_bits_to_f64(x)
+        amax = np.abs(xf).reshape(x.shape[0], -1, 32).max(2)
+        s2 = np.where(amax > 0, np.ceil(np.log2(np.where(amax > 0, amax, 1))) - 8 + 127, 0)
+        s2 = s2.astype(np.uint8)
+        X = np.ldexp(1.0, s2.astype(np.int64) - 127).repeat(32, 1)
+        q = np.array([[oracle.f32_to_e4m3(float(v)) for v in row] for row in xf / X], np.uint8)
+        return q, s2
+
+    def scale_once(xq, sx, perm, offsets, wq, sw, k, rows):   # W's block scales dropped
+        return oracle.gemm_mx_rows(xq, sx, perm, offsets, wq, np.full_like(sw, 127), k, rows)
+
+    def blocks_along_n(xq, sx, perm, offsets, wq, sw, k, rows):  # scale of block n // 32, not d // 32
+        E, N, nb = sw.shape
+        sw2 = np.ascontiguousarray(np.broadcast_to(sw[:, :, :1], sw.shape))
+        return oracle.gemm_mx_rows(xq, sx, perm, offsets, wq, sw2, k, rows)
+
+    for bad in (emax7, ceil_exp):
+        with pytest.raises(AssertionError):
+            check_mx_quant_rows(bad, np.random.default_rng(41))
+    for bad in (scale_once, blocks_along_n):
+        with pytest.raises(AssertionError):
+            check_gemm_mx(bad, np.random.default_rng(43))
