@@ -615,6 +615,33 @@ def run_op(args, wl):
         flops = 2.0 * R * wl.D * wl.De
         metric = (f"FP8 (E4M3) dispatch + expert GEMM TFLOP/s at T={wl.T} D={wl.D} E={wl.E} "
                   f"k={wl.k} D_expert={wl.De}")
+    elif args.op == "mxfp8_gemm":
+        # MXFP8: E4M3 codes with one E8M0 scale per 32 elements along D, on
+        # block-scaled tensor-core MMAs; weights quantised once, outside the
+        # timed region, as a model would at load time
+        x = dev_bf16(ig.make_x(wl))
+        W = dev_bf16(ig.make_W(wl))
+        wq = torch.empty((pk.pk_moe_fp8_weight_bytes(wl.E, wl.D, wl.De),), dtype=torch.uint8,
+                         device=dev)
+        swb = torch.empty((pk.pk_moe_mx_weight_scale_bytes(wl.E, wl.D, wl.De),), dtype=torch.uint8,
+                          device=dev)
+        pk.pk_moe_quant_weights_mx(W, wq, swb, stream)
+        del W
+        xq = torch.empty((wl.T, wl.D), dtype=torch.uint8, device=dev)
+        sx = torch.empty((wl.T, wl.D // 32), dtype=torch.uint8, device=dev)
+        pk.pk_moe_quant_rows_mx(x, xq, sx, stream)
+        out = torch.empty((R, wl.De), dtype=torch.bfloat16, device=dev)
+        fn = lambda: pk.pk_moe_dispatch_gemm_mxfp8(xq, sx, md.perm, md.offsets, wq, swb, wl.E,
+                                                   wl.De, wl.k, out, md.status, stream)
+        qfn = lambda: pk.pk_moe_quant_rows_mx(x, xq, sx, stream)
+        touched = int((counts > 0).sum())
+        # codes and scale bytes of the touched experts' W, x codes and scale
+        # bytes gathered per routed row, out, perm, offsets
+        alg_bytes = (R * wl.D + R * (wl.D // 32) + touched * wl.D * wl.De
+                     + touched * wl.De * (wl.D // 32) + R * wl.De * 2 + R * 4 + (wl.E + 1) * 4)
+        flops = 2.0 * R * wl.D * wl.De
+        metric = (f"MXFP8 (E4M3, E8M0 per 32) dispatch + expert GEMM TFLOP/s at T={wl.T} "
+                  f"D={wl.D} E={wl.E} k={wl.k} D_expert={wl.De}")
     elif args.op == "fp8_grouped_gemm":
         # FP8 down-projection: h quantised per row, W2 per (expert, column), once
         K, N = wl.De, wl.D
@@ -655,7 +682,8 @@ def run_op(args, wl):
     op_profile = {"combine": ("combine", "combine_router.cu"),
                   "grouped_gemm": ("grouped_gemm", "dispatch_gemm.cu"),
                   "fp8_gemm": ("fp8_dispatch_gemm", "dispatch_gemm.cu"),
-                  "fp8_grouped_gemm": ("fp8_grouped_gemm", "dispatch_gemm.cu")}.get(args.op)
+                  "fp8_grouped_gemm": ("fp8_grouped_gemm", "dispatch_gemm.cu"),
+                  "mxfp8_gemm": ("mxfp8_dispatch_gemm", "dispatch_gemm.cu")}.get(args.op)
     traffic = (profiled_traffic(wl.name, prefix=op_profile[0], src=op_profile[1])
                if op_profile else None)
     line = {"op": args.op, "metric": metric, "workload": wl.name, "ms_median": med,
@@ -667,7 +695,7 @@ def run_op(args, wl):
         tf = flops / (med * 1e-3) / 1e12
         line["value"], line["unit"] = tf, "TFLOP/s"
         # FP8 peak: the measured bf16 peak times the nominal fp8/bf16 ratio (4.5 / 2.25)
-        fp8_op = args.op in ("fp8_gemm", "fp8_grouped_gemm")
+        fp8_op = args.op in ("fp8_gemm", "fp8_grouped_gemm", "mxfp8_gemm")
         tpeak = peaks["bf16_tflops"] * (2.0 if fp8_op else 1.0)
         line["roofline"]["tensor"] = {"achieved": tf, "peak": tpeak, "unit": "TFLOP/s",
                                       "frac": tf / tpeak}
@@ -702,7 +730,7 @@ def main(argv=None):
                          "(2-CTA clusters)")
     ap.add_argument("--op", default="dispatch_gemm",
                     choices=["dispatch_gemm", "router", "combine", "grouped_gemm", "fp8_gemm",
-                             "fp8_grouped_gemm"],
+                             "fp8_grouped_gemm", "mxfp8_gemm"],
                     help="dispatch_gemm: the benchmark step; the others time one kernel")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)

@@ -68,7 +68,7 @@ const char* pk_status_str(int status);
 /* Version of this ABI (major * 10000 + minor * 100 + patch). 1.1: FP8
  * entry points (quantisation, dispatch and grouped GEMM), GEMM kernel
  * selection, routing launch count. 1.2: PK_ERR_CAPTURE, the GEMM stall test
- * hook. */
+ * hook, MXFP8 quantisation and dispatch GEMM. */
 #define PK_ABI_VERSION 10200
 int pk_abi_version(void);
 
@@ -199,6 +199,48 @@ int pk_moe_quant_rows(const uint16_t* x, int32_t T, int32_t D, uint8_t* xq, floa
 size_t pk_moe_fp8_weight_bytes(int32_t E, int32_t D, int32_t N);
 int pk_moe_quant_weights(const uint16_t* W, int32_t E, int32_t D, int32_t N, uint8_t* wq,
                          float* sw, void* stream);
+
+/*
+ * Microscaled FP8 (MXFP8) form of the expert GEMM: the "Microscaling FP8"
+ * tensor-core primitive named by the "ThunderKittens 2.0 & FP8/NVFP4" item of
+ * the ThunderKittens tutorial page; the format follows the definition of the
+ * MX formats. Along D, every 32 consecutive elements share one power-of-two
+ * scale 2^s stored as an E8M0 byte s + 127, with
+ *   s = floor(log2(max |v|)) - 8 (clamped to [-127, 127]; -127 for an
+ *       all-zero block),  code = E4M3_rne_satfinite(v * 2^-s)  (in fp32).
+ *
+ * pk_moe_quant_rows_mx: x device bf16 [T, D], D a multiple of 32, 16-byte
+ *   aligned -> xq device uint8 [T, D] codes (16-byte aligned) and sx device
+ *   uint8 [T, D / 32] scale bytes (block b of row t covers d in [32 b, 32 b+32)).
+ * pk_moe_quant_weights_mx: W device bf16 [E, D, N], D a multiple of 128, N a
+ *   multiple of 8, all pointers 16-byte aligned -> wq: codes of the columns of
+ *   every W[e] in the blocked layout of pk_moe_quant_weights
+ *   (pk_moe_fp8_weight_bytes(E, D, N) bytes); swb: the blocks' scale bytes,
+ *   pk_moe_mx_weight_scale_bytes(E, D, N) bytes, laid out for the GEMM: one
+ *   1 KiB piece per (expert e, tile of 192 columns t, group of 128 d ks) at
+ *   ((e * ceil(N / 192) + t) * (D / 128) + ks) * 1024; in it, bytes
+ *   h * 512 + r * 16 + g * 4 + j hold the scale of block 4 ks + j of column
+ *   192 t + 128 h + 32 g + r (h < 2, r < 32, g < 4); other bytes are zero.
+ * pk_moe_dispatch_gemm_mxfp8: for every expert e and sorted row j in
+ *   [expert_offsets[e], expert_offsets[e+1]),
+ *     out[j, n] = bf16_rne( sum_d (q(x)[t, d] * 2^sx[t, d/32])
+ *                                * (q(W)[e, d, n] * 2^sw[e, n, d/32]) ),
+ *   t = perm[j] / k, on block-scaled tensor-core MMAs with fp32 accumulation.
+ *   xq, wq, swb from the two calls above (xq, wq, swb, out 16-byte aligned,
+ *   sx 4-byte aligned); D a multiple of 128, D_expert of 8. Otherwise as
+ *   pk_moe_dispatch_gemm (clamped offsets, PK_ERR_BAD_INDEX for a perm entry
+ *   outside [0, T*k)). Always the one-CTA kernel.
+ */
+int pk_moe_quant_rows_mx(const uint16_t* x, int32_t T, int32_t D, uint8_t* xq, uint8_t* sx,
+                         void* stream);
+size_t pk_moe_mx_weight_scale_bytes(int32_t E, int32_t D, int32_t N);
+int pk_moe_quant_weights_mx(const uint16_t* W, int32_t E, int32_t D, int32_t N, uint8_t* wq,
+                            uint8_t* swb, void* stream);
+int pk_moe_dispatch_gemm_mxfp8(const uint8_t* xq, const uint8_t* sx, const int32_t* perm,
+                               const int32_t* expert_offsets, const uint8_t* wq,
+                               const uint8_t* swb, int32_t T, int32_t k, int32_t D, int32_t E,
+                               int32_t D_expert, uint16_t* out, int32_t* status_word,
+                               void* stream);
 
 /*
  * Grouped GEMM of rows already in expert order -- the expert MLP's

@@ -27,6 +27,10 @@ from ._binding import (  # noqa: F401
     pk_abi_version,
     pk_debug_bounded_wait,
     pk_debug_stall_gemm,
+    pk_moe_dispatch_gemm_mxfp8,
+    pk_moe_mx_weight_scale_bytes,
+    pk_moe_quant_rows_mx,
+    pk_moe_quant_weights_mx,
     pk_moe_build_perm,
     pk_moe_combine,
     pk_moe_dispatch_gemm,

@@ -79,6 +79,14 @@ def _load():
     lib.pk_moe_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
     lib.pk_debug_bounded_wait.restype = ctypes.c_int
     lib.pk_debug_bounded_wait.argtypes = [P, ctypes.c_uint64, P]
+    lib.pk_moe_quant_rows_mx.restype = ctypes.c_int
+    lib.pk_moe_quant_rows_mx.argtypes = [P, I32, I32, P, P, P]
+    lib.pk_moe_mx_weight_scale_bytes.restype = SZ
+    lib.pk_moe_mx_weight_scale_bytes.argtypes = [I32, I32, I32]
+    lib.pk_moe_quant_weights_mx.restype = ctypes.c_int
+    lib.pk_moe_quant_weights_mx.argtypes = [P, I32, I32, I32, P, P, P]
+    lib.pk_moe_dispatch_gemm_mxfp8.restype = ctypes.c_int
+    lib.pk_moe_dispatch_gemm_mxfp8.argtypes = [P, P, P, P, P, P, I32, I32, I32, I32, I32, P, P, P]
     lib.pk_debug_stall_gemm.restype = None
     lib.pk_debug_stall_gemm.argtypes = [I32, ctypes.c_int64]
     return lib
@@ -235,6 +243,52 @@ def pk_moe_quant_weights(W: torch.Tensor, wq: torch.Tensor, sw: torch.Tensor,
                                   _ptr(wq, torch.uint8, "wq", pk_moe_fp8_weight_bytes(E, D, N)),
                                   _ptr(sw, torch.float32, "sw", E * N), _stream(stream))
     _check(rc, "pk_moe_quant_weights")
+
+
+def pk_moe_quant_rows_mx(x: torch.Tensor, xq: torch.Tensor, sx: torch.Tensor,
+                         stream=None) -> None:
+    """x: bf16 [T, D] -> xq uint8 E4M3 codes [T, D], sx uint8 E8M0 scale bytes
+    [T, D // 32]."""
+    T, D = x.shape
+    rc = lib.pk_moe_quant_rows_mx(_ptr(x, torch.bfloat16, "x"), T, D,
+                                  _ptr(xq, torch.uint8, "xq", T * D),
+                                  _ptr(sx, torch.uint8, "sx", T * (D // 32)), _stream(stream))
+    _check(rc, "pk_moe_quant_rows_mx")
+
+
+def pk_moe_mx_weight_scale_bytes(E: int, D: int, N: int) -> int:
+    return int(lib.pk_moe_mx_weight_scale_bytes(E, D, N))
+
+
+def pk_moe_quant_weights_mx(W: torch.Tensor, wq: torch.Tensor, swb: torch.Tensor,
+                            stream=None) -> None:
+    """W: bf16 [E, D, N] -> wq uint8 blocked codes (pk_moe_fp8_weight_bytes
+    bytes), swb uint8 scale pieces (pk_moe_mx_weight_scale_bytes bytes)."""
+    E, D, N = W.shape
+    rc = lib.pk_moe_quant_weights_mx(
+        _ptr(W, torch.bfloat16, "W"), E, D, N,
+        _ptr(wq, torch.uint8, "wq", pk_moe_fp8_weight_bytes(E, D, N)),
+        _ptr(swb, torch.uint8, "swb", pk_moe_mx_weight_scale_bytes(E, D, N)), _stream(stream))
+    _check(rc, "pk_moe_quant_weights_mx")
+
+
+def pk_moe_dispatch_gemm_mxfp8(xq: torch.Tensor, sx: torch.Tensor, perm: torch.Tensor,
+                               expert_offsets: torch.Tensor, wq: torch.Tensor,
+                               swb: torch.Tensor, E: int, D_expert: int, k: int,
+                               out: torch.Tensor, status_word: torch.Tensor | None = None,
+                               stream=None) -> None:
+    """xq, sx from pk_moe_quant_rows_mx; wq, swb from pk_moe_quant_weights_mx."""
+    T, D = xq.shape
+    De = D_expert
+    rc = lib.pk_moe_dispatch_gemm_mxfp8(
+        _ptr(xq, torch.uint8, "xq"), _ptr(sx, torch.uint8, "sx", T * (D // 32)),
+        _ptr(perm, torch.int32, "perm", T * k),
+        _ptr(expert_offsets, torch.int32, "expert_offsets", E + 1),
+        _ptr(wq, torch.uint8, "wq", pk_moe_fp8_weight_bytes(E, D, De)),
+        _ptr(swb, torch.uint8, "swb", pk_moe_mx_weight_scale_bytes(E, D, De)), T, k, D, E, De,
+        _ptr(out, torch.bfloat16, "out", T * k * De),
+        _ptr(status_word, torch.int32, "status_word", 1), _stream(stream))
+    _check(rc, "pk_moe_dispatch_gemm_mxfp8")
 
 
 def pk_moe_grouped_gemm_fp8(Aq: torch.Tensor, sa: torch.Tensor, expert_offsets: torch.Tensor,

@@ -153,6 +153,52 @@ int pk_moe_quant_weights(const uint16_t* W, int32_t E, int32_t D, int32_t N, uin
     return err == cudaSuccess ? PK_OK : PK_ERR_CUDA;
 }
 
+int pk_moe_quant_rows_mx(const uint16_t* x, int32_t T, int32_t D, uint8_t* xq, uint8_t* sx,
+                         void* stream) {
+    if (T < 0 || D < 1 || (D % 32) != 0) return PK_ERR_INVALID_ARG;
+    if (T == 0) return PK_OK;
+    if (!x || !xq || !sx) return PK_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(xq)) return PK_ERR_INVALID_ARG;
+    cudaError_t err = pk::launch_quant_rows_mx(x, T, D, xq, sx, static_cast<cudaStream_t>(stream));
+    return err == cudaSuccess ? PK_OK : PK_ERR_CUDA;
+}
+
+size_t pk_moe_mx_weight_scale_bytes(int32_t E, int32_t D, int32_t N) {
+    if (E < 1 || D < 128 || (D % 128) != 0 || N < 1) return 0;
+    return pk::mx_weight_scale_bytes(E, D, N);
+}
+
+int pk_moe_quant_weights_mx(const uint16_t* W, int32_t E, int32_t D, int32_t N, uint8_t* wq,
+                            uint8_t* swb, void* stream) {
+    if (E < 1 || D < 1 || N < 1 || (D % 128) != 0 || (N % 8) != 0) return PK_ERR_INVALID_ARG;
+    if (E > 65535) return PK_ERR_UNSUPPORTED;  // experts are a grid dimension
+    if (!W || !wq || !swb) return PK_ERR_INVALID_ARG;
+    if (!aligned16(W) || !aligned16(wq) || !aligned16(swb)) return PK_ERR_INVALID_ARG;
+    cudaError_t err =
+        pk::launch_quant_cols_mx(W, E, D, N, wq, swb, static_cast<cudaStream_t>(stream));
+    return err == cudaSuccess ? PK_OK : PK_ERR_CUDA;
+}
+
+int pk_moe_dispatch_gemm_mxfp8(const uint8_t* xq, const uint8_t* sx, const int32_t* perm,
+                               const int32_t* expert_offsets, const uint8_t* wq,
+                               const uint8_t* swb, int32_t T, int32_t k, int32_t D, int32_t E,
+                               int32_t D_expert, uint16_t* out, int32_t* status_word,
+                               void* stream) {
+    if (T < 0 || k < 1 || E < 1 || D < 1 || D_expert < 1) return PK_ERR_INVALID_ARG;
+    if ((D % 128) != 0 || (D_expert % 8) != 0) return PK_ERR_INVALID_ARG;
+    const int64_t R = static_cast<int64_t>(T) * k;
+    if (R >= (int64_t{1} << 31)) return PK_ERR_UNSUPPORTED;
+    if (R == 0) return PK_OK;
+    if (!xq || !sx || !perm || !expert_offsets || !wq || !swb || !out) return PK_ERR_INVALID_ARG;
+    if (!aligned16(xq) || !aligned16(wq) || !aligned16(swb) || !aligned16(out) ||
+        (reinterpret_cast<uintptr_t>(sx) & 3u) != 0)
+        return PK_ERR_INVALID_ARG;
+    if (pk_moe_fp8_weight_bytes(E, D, D_expert) >= (size_t{1} << 38)) return PK_ERR_UNSUPPORTED;
+    return pk::launch_dispatch_gemm_mx(xq, sx, perm, expert_offsets, wq, swb, T, k, D, E, D_expert,
+                                       out, status_word, static_cast<cudaStream_t>(stream),
+                                       g_wait_limit_ns.load(std::memory_order_relaxed));
+}
+
 int pk_moe_grouped_gemm(const uint16_t* A, const int32_t* expert_offsets, const uint16_t* W,
                         int32_t R, int32_t K, int32_t N, int32_t E, uint16_t* out,
                         int32_t* status_word, void* stream) {

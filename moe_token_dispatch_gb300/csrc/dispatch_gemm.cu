@@ -113,6 +113,17 @@ constexpr int RING_BYTES = A_RING_OFF + A_STAGES * A_SLOT;   // 224 KiB
 constexpr int NBAR = 8;
 static_assert(NBAR > W_STAGES && NBAR > A_STAGES, "barrier ring shorter than a slot lag");
 constexpr int UMMA_K = 16;
+// MXFP8 (kMx): units of at most two m-tiles and 192 columns, so that the
+// accumulators (384 TMEM columns) leave room for four 16-column buffers of
+// block scales (one per A slot); each K-step's scales travel in the W slot
+// after its 24 KiB of codes: W's (two 512-byte halves, 1 KiB) then the rows'
+// (512 bytes per m-tile).
+constexpr int MX_BN = 192;
+constexpr int MX_SFB_OFF = MX_BN * ROW_BYTES;        // 24 KiB into the W slot
+constexpr int MX_SFA_OFF = MX_SFB_OFF + 1024;
+constexpr uint32_t MX_SF_TMEM = 2 * MX_BN;           // first scale column in TMEM
+constexpr uint32_t MX_SF_COLS = 16;                  // per buffer: A m-tiles 0, 1, B halves
+static_assert(MX_SFA_OFF + 2 * 512 <= W_SLOT, "MX scales fit the W slot");
 constexpr uint32_t TMEM_COLS = 512;
 
 constexpr int EPI_WARPS = 4;                 // warps 0..3
@@ -324,14 +335,21 @@ __device__ __forceinline__ void scale_chunk(uint32_t (&v)[32], float rs, float c
         v[j] = __float_as_uint((__uint_as_float(v[j]) * rs) * __shfl_sync(0xffffffffu, cs, j));
 }
 
-template <bool kGather, bool kFp8>
+// kMx (with kGather and kFp8): E4M3 codes with one E8M0 scale per 32 codes
+// along D: sx_ is the rows' scale bytes [T, D / 32], sw_ the weights' scale
+// pieces (1 KiB per 192-column tile and K-step); otherwise (FP8) both are
+// fp32 scales [T] and [E, De].
+template <bool kGather, bool kFp8, bool kMx = false>
 __global__ void __launch_bounds__(THREADS, 1)
     k_dispatch_gemm(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap amap,
-                    const uint8_t* __restrict__ x, const float* __restrict__ sx,
-                    const float* __restrict__ sw,
+                    const uint8_t* __restrict__ x, const void* __restrict__ sx_,
+                    const void* __restrict__ sw_,
                     const int32_t* __restrict__ perm, const int32_t* __restrict__ offsets,
                     uint16_t* __restrict__ out, int32_t T, int32_t k, int32_t D, int32_t E,
                     int32_t De, int32_t* status, uint64_t limit, int64_t stall) {
+    static_assert(!kMx || (kGather && kFp8), "MXFP8 is a form of the FP8 dispatch GEMM");
+    const float* sx = static_cast<const float*>(sx_);
+    const float* sw = static_cast<const float*>(sw_);
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t sbase = (raw + 1023u) & ~1023u;
@@ -458,6 +476,61 @@ __global__ void __launch_bounds__(THREADS, 1)
         // Copies still in flight must land before the CTA may exit.
         cp_async_wait_all();
         if (bad) report(status, PK_ERR_BAD_INDEX);
+    } else if (kMx && warp == GATHER2_WARP) {
+        // --------------------------- MX: the rows' block scales, per K-step
+        // Four scale bytes (the K-step's four 32-code blocks) of each row's
+        // token, into the W slot as the 32-row x 16-byte pieces that
+        // tcgen05.cp copies: row r of m-tile mt at byte (r % 32) * 16 +
+        // (r / 32 % 4) * 4 of piece mt. Lane l takes rows l + 32 i.
+        const uint8_t* sxm = static_cast<const uint8_t*>(sx_);
+        const int nbr = D / 32;                   // scale bytes per token row
+        Cursor<NQ> qc;
+        Cursor<NBAR> bc;
+        Cursor<W_STAGES> wc;
+        Cursor<NBAR> back = lag_cursor<W_STAGES>();  // the W slot's previous user
+        bool ok = true, bad = false;
+        while (ok) {
+            Unit U;
+            const int got = q_pop<true>(qfull0, qempty0, ctl->q, qc, U, abort, limit);
+            if (got <= 0) {
+                if (got < 0 && lane == 0) fail(abort, status);
+                break;
+            }
+            int tok[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int r = lane + 32 * i;
+                int t = -1;
+                if (r < U.rows) {
+                    int f = __ldg(perm + U.row0 + r);
+                    if (f < 0 || f >= R) {
+                        bad = true;
+                        f = 0;
+                    }
+                    t = f / k;
+                }
+                tok[i] = t;
+            }
+            for (int ks = 0; ks < nk; ++ks) {
+                if (!warp_wait(wempty0 + 8 * back.s, back.ph, abort, limit)) {
+                    if (lane == 0) fail(abort, status);
+                    ok = false;
+                    break;
+                }
+                const uint32_t dst0 = sbase + wc.s * W_SLOT + MX_SFA_OFF + lane * 16;
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    if (tok[i] >= 0)
+                        cp_async_4(dst0 + (i >> 2) * 512 + (i & 3) * 4,
+                                   sxm + static_cast<int64_t>(tok[i]) * nbr + 4 * ks);
+                cp_async_arrive_noinc(wfull0 + 8 * bc.s);
+                bc.next();
+                wc.next();
+                back.next();
+            }
+        }
+        cp_async_wait_all();
+        if (bad) report(status, PK_ERR_BAD_INDEX);
     } else if (kGather && warp == GATHER2_WARP) {
         // -------------------------- dispatch, m-tile 2 of 3-m-tile units
         // Its own warp, so that its shorter lead (it writes the W slot's
@@ -557,7 +630,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                 // grouped GEMM: m-tiles 0, 1 to the A slot, m-tile 2 to the W slot
                 const int a_lo = U.mpu < 2 ? U.mpu : 2;
                 const uint32_t wtx = static_cast<uint32_t>(nbox * B_BOX_BYTES) +
-                                     (!kGather && U.mpu > 2 ? static_cast<uint32_t>(A_BYTES) : 0u);
+                                     (!kGather && U.mpu > 2 ? static_cast<uint32_t>(A_BYTES) : 0u) +
+                                     (kMx ? 1024u : 0u);
                 const uint32_t atx = static_cast<uint32_t>(a_lo * A_BYTES);
                 for (int ks = 0; ks < nk; ++ks) {
                     if (!mbar_wait(wempty0 + 8 * back.s, back.ph, abort, limit)) {
@@ -579,6 +653,12 @@ __global__ void __launch_bounds__(THREADS, 1)
                             tma_load_3d(wsl + b * B_BOX_BYTES, &wmap, U.n0 + b * B_BOX, ks * BKE,
                                         U.e, wfull, pol);
                     }
+                    if (kMx && !stalled)  // W's block scales of this tile and K-step
+                        bulk_g2s(wsl + MX_SFB_OFF,
+                                 static_cast<const uint8_t*>(sw_) +
+                                     ((static_cast<int64_t>(U.e) * ((De + MX_BN - 1) / MX_BN) +
+                                       U.n0 / MX_BN) * nk + ks) * 1024,
+                                 1024u, wfull, pol);
                     if (!stalled) {
                         w_issued |= 1u << bc.s;
                         w_par = (w_par & ~(1u << bc.s)) | (bc.ph << bc.s);
@@ -646,12 +726,28 @@ __global__ void __launch_bounds__(THREADS, 1)
                     // order them before the tensor cores' async-proxy reads.
                     fence_proxy_async_smem();
                     const uint64_t b_st = b_desc0 + ((sbase + wc.s * W_SLOT) >> 4);
+                    // MX: this K-step's scales into TMEM buffer ac.s (its last
+                    // reader, the K-step A_STAGES back, has completed: the rows
+                    // of this K-step could only be gathered after it)
+                    const uint32_t sft = tmem + MX_SF_TMEM + MX_SF_COLS * static_cast<uint32_t>(ac.s);
+                    if (kMx) {
+                        const uint32_t sfs = sbase + wc.s * W_SLOT + MX_SFB_OFF;
+                        tmem_cp_32x128b_x4(sft + 8, sdesc_plain(sfs, 0, 128));
+                        tmem_cp_32x128b_x4(sft + 12, sdesc_plain(sfs + 512, 0, 128));
+                        for (int mt = 0; mt < mpu; ++mt)
+                            tmem_cp_32x128b_x4(sft + 4 * mt,
+                                               sdesc_plain(sfs + 1024 + 512 * mt, 0, 128));
+                    }
                     for (int mt = 0; mt < mpu; ++mt) {
                         const uint64_t a_mt = a_desc0 + (a_tile(wc.s, ac.s, mt) >> 4);
                         const uint32_t d = tmem + static_cast<uint32_t>(mt) * acc_stride;
 #pragma unroll
                         for (int kk = 0; kk < 4; ++kk) {  // four K steps of 32 bytes per K-step
-                            if (kFp8)
+                            if (kMx)
+                                mma_mx(d, a_mt + kk * (32 >> 4), b_st + kk * b_step,
+                                       idesc_mx_e4m3(BM, U.bn, kk), sft + 4 * mt, sft + 8,
+                                       (ks | kk) != 0 ? 1u : 0u);
+                            else if (kFp8)
                                 mma_f8(d, a_mt + kk * (32 >> 4), b_st + kk * b_step, idesc,
                                        (ks | kk) != 0 ? 1u : 0u);
                             else
@@ -690,7 +786,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             // (one per 32 columns), loaded while the unit's MMAs still run.
             float rs_pre[MAX_MPU] = {1.0f, 1.0f, 1.0f};
             float cs_pre[8] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
-            if (kFp8) {
+            if (kFp8 && !kMx) {
 #pragma unroll
                 for (int mt = 0; mt < MAX_MPU; ++mt) {
                     const int r = mt * BM + q * 32 + lane;
@@ -751,7 +847,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                         if (lane == 0) mbar_arrive(acc_empty);
                         released = true;
                     }
-                    if (kFp8) {  // all lanes: the scales travel by shuffles
+                    if (kFp8 && !kMx) {  // all lanes: the scales travel by shuffles
                         scale_chunk(v0, rs, cs0);
                         scale_chunk(v1, rs, cs1);
                     }
@@ -779,6 +875,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         // ...) 32 experts at a time, one expert per lane, and queues each
         // unit's descriptor; a descriptor with e = -1 ends the list.
         const int nt256 = (De + 255) >> 8, nt128 = (De + 127) >> 7;
+        const int ntmx = (De + MX_BN - 1) / MX_BN;
         int e0 = -32;
         int64_t before = 0, total = 0, cum = 0, units = 0;
         int lo = 0, rows = 0, mpu_max = 2, bn_max = 256, groups = 0, ntiles = 1;
@@ -801,7 +898,9 @@ __global__ void __launch_bounds__(THREADS, 1)
                     const int hi = min(max(__ldg(offsets + e + 1), 0), R);
                     rows = max(hi, lo) - lo;
                     const int mt = (rows + BM - 1) / BM;
-                    if (mt == 3) {
+                    if (kMx) {
+                        mpu_max = 2; bn_max = MX_BN; groups = (mt + 1) >> 1; ntiles = ntmx;
+                    } else if (mt == 3) {
                         mpu_max = 3; bn_max = 128; groups = 1; ntiles = nt128;
                     } else {
                         mpu_max = 2; bn_max = 256; groups = (mt + 1) >> 1; ntiles = nt256;
@@ -932,11 +1031,12 @@ namespace {
 // Builds the tensor maps and launches one instantiation. A is x (gathered
 // through perm) or, without gather, the [T, D] matrix of expert-sorted rows.
 // fp8: x and W are E4M3 codes (W blocked, see pk_moe_fp8_weight_bytes) with
-// scales sx [T], sw [E, De].
-int launch_common(bool gather, bool fp8, const void* A, const float* sx, const int32_t* perm,
-                  const int32_t* offsets, const void* W, const float* sw, int32_t T, int32_t k,
+// scales sx [T], sw [E, De] (fp32), or with mx, E8M0 block scales (sx the
+// rows' bytes [T, D / 32], sw the weights' scale pieces).
+int launch_common(bool gather, bool fp8, const void* A, const void* sx, const int32_t* perm,
+                  const int32_t* offsets, const void* W, const void* sw, int32_t T, int32_t k,
                   int32_t D, int32_t E, int32_t De, uint16_t* out, int32_t* status,
-                  cudaStream_t stream, uint64_t wait_limit_ns) {
+                  cudaStream_t stream, uint64_t wait_limit_ns, bool mx = false) {
     const int64_t stall = g_debug_stall.load(std::memory_order_relaxed);
     using namespace dg;
     auto enc = encoder();
@@ -960,6 +1060,9 @@ int launch_common(bool gather, bool fp8, const void* A, const float* sx, const i
                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      SMEM_BYTES) != cudaSuccess ||
                 cudaFuncSetAttribute(k_dispatch_gemm<false, true>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     SMEM_BYTES) != cudaSuccess ||
+                cudaFuncSetAttribute(k_dispatch_gemm<true, true, true>,
                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      SMEM_BYTES) != cudaSuccess)
                 return PK_ERR_CUDA;
@@ -988,7 +1091,10 @@ int launch_common(bool gather, bool fp8, const void* A, const float* sx, const i
             return PK_ERR_UNSUPPORTED;
     }
     const uint8_t* a8 = static_cast<const uint8_t*>(A);
-    if (fp8 && gather)
+    if (mx)
+        k_dispatch_gemm<true, true, true><<<sms, THREADS, SMEM_BYTES, stream>>>(
+            wmap, amap, a8, sx, sw, perm, offsets, out, T, k, D, E, De, status, wait_limit_ns, stall);
+    else if (fp8 && gather)
         k_dispatch_gemm<true, true><<<sms, THREADS, SMEM_BYTES, stream>>>(
             wmap, amap, a8, sx, sw, perm, offsets, out, T, k, D, E, De, status, wait_limit_ns, stall);
     else if (fp8)
@@ -1022,6 +1128,14 @@ int launch_dispatch_gemm_fp8_single(const uint8_t* xq, const float* sx, const in
                                     uint64_t wait_limit_ns) {
     return launch_common(true, true, xq, sx, perm, offsets, wq, sw, T, k, D, E, De, out, status,
                          stream, wait_limit_ns);
+}
+
+int launch_dispatch_gemm_mx(const uint8_t* xq, const uint8_t* sx, const int32_t* perm,
+                            const int32_t* offsets, const uint8_t* wq, const uint8_t* swb,
+                            int32_t T, int32_t k, int32_t D, int32_t E, int32_t De, uint16_t* out,
+                            int32_t* status, cudaStream_t stream, uint64_t wait_limit_ns) {
+    return launch_common(true, true, xq, sx, perm, offsets, wq, swb, T, k, D, E, De, out, status,
+                         stream, wait_limit_ns, true);
 }
 
 void set_debug_stall(int32_t cta, int64_t kstep) {

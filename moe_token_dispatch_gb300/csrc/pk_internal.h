@@ -67,6 +67,20 @@ int launch_grouped_gemm(const uint16_t* A, const int32_t* offsets, const uint16_
                         int32_t K, int32_t N, int32_t E, uint16_t* out, int32_t* status,
                         cudaStream_t stream, uint64_t wait_limit_ns);
 
+// MXFP8: E4M3 codes with one E8M0 scale byte per 32 elements along D.
+// Rows of x: codes [T, D], scales [T, D / 32]. Weights: codes in the FP8
+// blocked layout, scales in the blocked layout of the MX GEMM (D % 128 == 0).
+size_t mx_weight_scale_bytes(int32_t E, int32_t D, int32_t N);
+cudaError_t launch_quant_rows_mx(const uint16_t* x, int32_t T, int32_t D, uint8_t* q, uint8_t* s,
+                                 cudaStream_t stream);
+cudaError_t launch_quant_cols_mx(const uint16_t* W, int32_t E, int32_t D, int32_t N, uint8_t* q,
+                                 uint8_t* sb, cudaStream_t stream);
+// MXFP8 dispatch GEMM (block-scaled tensor-core MMAs).
+int launch_dispatch_gemm_mx(const uint8_t* xq, const uint8_t* sx, const int32_t* perm,
+                            const int32_t* offsets, const uint8_t* wq, const uint8_t* swb,
+                            int32_t T, int32_t k, int32_t D, int32_t E, int32_t De, uint16_t* out,
+                            int32_t* status, cudaStream_t stream, uint64_t wait_limit_ns);
+
 cudaError_t launch_bounded_wait_probe(int32_t* status, uint64_t limit_ns, cudaStream_t stream);
 // Test hook of the one-CTA GEMM kernels: CTA `cta` skips the copies of its
 // K-step `kstep` (counted over its units); cta < 0 turns it off.

@@ -385,3 +385,72 @@ __device__ __forceinline__ void st_cluster_u32(uint32_t addr_cluster, uint32_t v
     asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr_cluster), "r"(v) : "memory");
 }
 }  // namespace pk
+
+namespace pk {
+// ------------------------------------------------------- microscaled FP8 (MX)
+// D[tmem] (+)= (A * 2^sa) * (B * 2^sb): E4M3 operands, one E8M0 scale per 32
+// K-elements of every row of A and every column of B (kind::mxf8f6f4,
+// scale_vec::1X), fp32 accumulate. The scales are read from TMEM: for row m
+// of A from lane m, column sa_tmem + m / 32; for column n of B, by the rows
+// of lane quarter q, from lane 32 q + n % 32, column sb_tmem + n / 32. Each
+// 32-bit cell holds four scale bytes; the instruction descriptor's scale ids
+// pick the byte (measured on GB300 with patterned scales).
+__device__ __forceinline__ void mma_mx(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                       uint32_t idesc, uint32_t sa_tmem, uint32_t sb_tmem,
+                                       uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.u32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], "
+        "[%5], p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sa_tmem), "r"(sb_tmem), "r"(accumulate)
+        : "memory");
+}
+
+// Instruction descriptor for kind::mxf8f6f4 with E4M3 A and B (format 0 in bits
+// 7..9 and 10..12), both K-major, E8M0 scales (bit 23), N >> 3 in bits 17..22,
+// M >> 4 in bits 24..28, the byte of B's and A's scale cells in bits 4..5 and
+// 29..30.
+__host__ __device__ constexpr uint32_t idesc_mx_e4m3(int M, int N, int sf_id) {
+    return (static_cast<uint32_t>(sf_id & 3) << 4) | (static_cast<uint32_t>(N >> 3) << 17) |
+           (1u << 23) | (static_cast<uint32_t>(M >> 4) << 24) |
+           (static_cast<uint32_t>(sf_id & 3) << 29);
+}
+
+// Shared-memory matrix descriptor without swizzle: start address, leading and
+// stride byte offsets (both >> 4), descriptor version 1 in bits 46..47.
+__device__ __forceinline__ uint64_t sdesc_plain(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+    d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+    d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+    d |= static_cast<uint64_t>(1) << 46;
+    return d;
+}
+
+// Copies a 32-row x 16-byte block of shared memory (rows 16 bytes apart; a
+// plain descriptor with 128-byte stride between 8-row groups) into TMEM
+// lanes 0..31, columns taddr .. taddr+3, and the same into the other three
+// lane quarters. Ordered with this thread's later tcgen05.mma.
+__device__ __forceinline__ void tmem_cp_32x128b_x4(uint32_t taddr, uint64_t sdesc) {
+    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)
+                 : "memory");
+}
+
+// Bulk copy global -> shared memory of `bytes` (multiple of 16, both
+// addresses 16-byte aligned), completion counted in bytes on `bar`.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
+                                         uint32_t bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1], %2, [%3], %4;" ::"r"(dst),
+        "l"(src), "r"(bytes), "r"(bar), "l"(policy)
+        : "memory");
+}
+
+// 4-byte global -> shared copy through the LSU path (tracked by the thread's
+// cp.async arrivals like cp_async_16).
+__device__ __forceinline__ void cp_async_4(uint32_t dst, const void* src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
+}
+}  // namespace pk

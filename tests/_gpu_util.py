@@ -101,3 +101,34 @@ def check_case(pk, x_u16, topk, W_u16, E, rows=None, W_dev=None, threads=None):
         got = bf16_dev_to_f64(res["out_dev"][torch.from_numpy(rows).cuda()])
         assert_gemm_close(got, want, rows)
     return res, ref
+
+
+def to_blocked(q):
+    """E4M3 codes [E, N, D] (column n's codes contiguous) into the blocked
+    layout of the C ABI: [E, ceil(N/64), ceil(D/128), 64, 128], zero-padded."""
+    E, N, D = q.shape
+    NB, KB = -(-N // 64), -(-D // 128)
+    p = np.zeros((E, NB * 64, KB * 128), dtype=np.uint8)
+    p[:, :N, :D] = q
+    return np.ascontiguousarray(p.reshape(E, NB, 64, KB, 128).transpose(0, 1, 3, 2, 4))
+
+
+def to_mx_scale_pieces(sw):
+    """E8M0 bytes [E, N, D // 32] of W's columns into the C ABI's scale pieces:
+    per (e, 192-column tile t, 128-code group ks) 1 KiB, byte h*512 + r*16 +
+    g*4 + j = scale of block 4 ks + j of column 192 t + 128 h + 32 g + r."""
+    E, N, nb = sw.shape
+    KS, NT = nb // 4, -(-N // 192)
+    out = np.zeros((E, NT, KS, 2, 32, 4, 4), dtype=np.uint8)   # e, t, ks, h, r, g, j
+    for t in range(NT):
+        for h in range(2):
+            for g in range(4):
+                if 128 * h + 32 * g >= 192:
+                    continue
+                n0 = 192 * t + 128 * h + 32 * g
+                n1 = min(n0 + 32, N)
+                if n1 <= n0:
+                    continue
+                blk = sw[:, n0:n1, :].reshape(E, n1 - n0, KS, 4)
+                out[:, t, :, h, : n1 - n0, g, :] = blk.transpose(0, 2, 1, 3)
+    return out.reshape(-1)

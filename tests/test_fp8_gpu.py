@@ -13,23 +13,14 @@ import torch
 
 import inputgen as ig
 import oracle
-from _gpu_util import assert_gemm_close, bf16_dev_to_f64, boundary_rows, u16_to_bf16_dev
+from _gpu_util import (assert_gemm_close, bf16_dev_to_f64, boundary_rows, to_blocked,
+                       u16_to_bf16_dev)
 
 pytestmark = pytest.mark.gpu
 
 
 def _u8_dev(a):
     return torch.from_numpy(np.ascontiguousarray(a, dtype=np.uint8)).cuda()
-
-
-def to_blocked(q):
-    """Codes [E, N, D] (column n's codes contiguous) into the blocked layout
-    of the C ABI: [E, ceil(N/64), ceil(D/128), 64, 128], zero-padded."""
-    E, N, D = q.shape
-    NB, KB = -(-N // 64), -(-D // 128)
-    p = np.zeros((E, NB * 64, KB * 128), dtype=np.uint8)
-    p[:, :N, :D] = q
-    return np.ascontiguousarray(p.reshape(E, NB, 64, KB, 128).transpose(0, 1, 3, 2, 4))
 
 
 def _gpu_quant_rows(pk, x_u16):
