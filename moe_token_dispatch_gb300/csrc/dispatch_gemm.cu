@@ -10,9 +10,10 @@
 //              round-to-nearest-even, masked 16-byte stores of valid rows and
 //              columns.
 //   warp 4     MMA issuer (one thread) and TMEM owner: tcgen05.mma M=128 x
-//              N=bn x K=16 per m-tile into fp32 accumulators in TMEM; each
-//              commit frees a shared-memory slot or hands the unit's
-//              accumulators to the epilogue.
+//              N=bn x K=16 per m-tile (M=64 for a last m-tile of at most 64
+//              rows) into fp32 accumulators in TMEM; each commit frees a
+//              shared-memory slot or hands the unit's accumulators to the
+//              epilogue.
 //   warp 5     W producer (one thread): per K-step of 64 rows, TMA-loads the
 //              W_e tile [64 x bn] as 64x64 boxes, 128-byte swizzle (MN-major
 //              operand).
@@ -113,6 +114,16 @@ constexpr int RING_BYTES = A_RING_OFF + A_STAGES * A_SLOT;   // 224 KiB
 constexpr int NBAR = 8;
 static_assert(NBAR > W_STAGES && NBAR > A_STAGES, "barrier ring shorter than a slot lag");
 constexpr int UMMA_K = 16;
+// A unit whose last m-tile holds at most 64 rows issues that m-tile's MMAs
+// with M = 64 (bf16 and FP8; not MX). An M = 64 MMA takes the tensor core as
+// long as an M = 128 one but does half the multiplies: on the power-capped
+// GB300 the saved energy raises the clock (ep: the 3-m-tile experts' third
+// m-tile holds ~13 of 128 rows). Its accumulator rows 16 q .. 16 q + 15 sit
+// in TMEM lanes 32 q .. 32 q + 15 (lane quarter q).
+constexpr int BM_HALF = 64;
+__device__ __forceinline__ bool half_last(int mpu, int rows) {
+    return rows - (mpu - 1) * BM <= BM_HALF;
+}
 // MXFP8 (kMx): units of at most two m-tiles and 192 columns, so that the
 // accumulators (384 TMEM columns) leave room for four 16-column buffers of
 // block scales (one per A slot); each K-step's scales travel in the W slot
@@ -713,6 +724,11 @@ __global__ void __launch_bounds__(THREADS, 1)
                 tc_fence_after_sync();
                 const uint32_t idesc =
                     kFp8 ? idesc_e4m3_f32(BM, U.bn) : idesc_bf16_f32(BM, U.bn, true);
+                const bool half = !kMx && half_last(U.mpu, U.rows);
+                const uint32_t idesc_last =
+                    !half ? idesc
+                          : (kFp8 ? idesc_e4m3_f32(BM_HALF, U.bn)
+                                  : idesc_bf16_f32(BM_HALF, U.bn, true));
                 const int mpu = U.mpu;
                 const uint32_t acc_stride = static_cast<uint32_t>(U.bn_max);
                 for (int ks = 0; ks < nk; ++ks) {
@@ -740,6 +756,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                     }
                     for (int mt = 0; mt < mpu; ++mt) {
                         const uint64_t a_mt = a_desc0 + (a_tile(wc.s, ac.s, mt) >> 4);
+                        const uint32_t id = mt == mpu - 1 ? idesc_last : idesc;
                         const uint32_t d = tmem + static_cast<uint32_t>(mt) * acc_stride;
 #pragma unroll
                         for (int kk = 0; kk < 4; ++kk) {  // four K steps of 32 bytes per K-step
@@ -748,10 +765,10 @@ __global__ void __launch_bounds__(THREADS, 1)
                                        idesc_mx_e4m3(BM, U.bn, kk), sft + 4 * mt, sft + 8,
                                        (ks | kk) != 0 ? 1u : 0u);
                             else if (kFp8)
-                                mma_f8(d, a_mt + kk * (32 >> 4), b_st + kk * b_step, idesc,
+                                mma_f8(d, a_mt + kk * (32 >> 4), b_st + kk * b_step, id,
                                        (ks | kk) != 0 ? 1u : 0u);
                             else
-                                mma_bf16(d, a_mt + kk * (32 >> 4), b_st + kk * b_step, idesc,
+                                mma_bf16(d, a_mt + kk * (32 >> 4), b_st + kk * b_step, id,
                                          (ks | kk) != 0 ? 1u : 0u);
                         }
                     }
@@ -784,13 +801,19 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
             // FP8: this lane's row scales (one per m-tile) and column scales
             // (one per 32 columns), loaded while the unit's MMAs still run.
+            // Rows of m-tile mt in this warp's lane quarter: 32 from row
+            // mt * BM + 32 q, or 16 from mt * BM + 16 q for an M = 64 last
+            // m-tile (its lanes 0..15).
+            const bool half = !kMx && half_last(U.mpu, U.rows);
+            auto qrows = [&](int mt) { return (half && mt == U.mpu - 1) ? 16 : 32; };
+            auto qrow0 = [&](int mt) { return mt * BM + qrows(mt) * q; };
             float rs_pre[MAX_MPU] = {1.0f, 1.0f, 1.0f};
             float cs_pre[8] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
             if (kFp8 && !kMx) {
 #pragma unroll
                 for (int mt = 0; mt < MAX_MPU; ++mt) {
-                    const int r = mt * BM + q * 32 + lane;
-                    if (mt < U.mpu && r < U.rows) {
+                    const int r = qrow0(mt) + lane;
+                    if (mt < U.mpu && lane < qrows(mt) && r < U.rows) {
                         if (kGather) {
                             const int f = __ldg(perm + U.row0 + r);
                             rs_pre[mt] = (f >= 0 && f < R) ? __ldg(sx + f / k) : 0.0f;
@@ -815,13 +838,13 @@ __global__ void __launch_bounds__(THREADS, 1)
             // after its last load, before its last stores.
             int last_mt = -1;
             for (int mt = 0; mt < U.mpu; ++mt)
-                if (mt * BM + q * 32 < U.rows) last_mt = mt;
+                if (qrow0(mt) < U.rows) last_mt = mt;
             bool released = false;
             for (int mt = 0; mt <= last_mt; ++mt) {
-                const int rbase = mt * BM + q * 32;
+                const int rbase = qrow0(mt);
                 if (rbase >= U.rows) continue;  // warp-uniform
                 const int r = rbase + lane;
-                const bool valid = r < U.rows;
+                const bool valid = lane < qrows(mt) && r < U.rows;
                 uint16_t* orow = out + static_cast<int64_t>(U.row0 + r) * De;
                 // FP8: this row's scale (its token's, or its own row's)
                 const float rs = mt == 0 ? rs_pre[0] : (mt == 1 ? rs_pre[1] : rs_pre[2]);
@@ -852,8 +875,9 @@ __global__ void __launch_bounds__(THREADS, 1)
                         scale_chunk(v1, rs, cs1);
                     }
                     if (wide) {
-                        store_rows_quad(out, static_cast<int64_t>(U.row0) + rbase, U.rows - rbase, De,
-                                        v0, v1, U.n0 + cc * 32);
+                        store_rows_quad(out, static_cast<int64_t>(U.row0) + rbase,
+                                        min(U.rows - rbase, qrows(mt)), De, v0, v1,
+                                        U.n0 + cc * 32);
                     } else if (valid) {
                         store_row_chunk(orow, v0, U.n0 + cc * 32, De, false);
                         store_row_chunk(orow, v1, U.n0 + cc * 32 + 32, De, false);

@@ -132,3 +132,19 @@ def to_mx_scale_pieces(sw):
                 blk = sw[:, n0:n1, :].reshape(E, n1 - n0, KS, 4)
                 out[:, t, :, h, : n1 - n0, g, :] = blk.transpose(0, 2, 1, 3)
     return out.reshape(-1)
+
+
+# Rows per expert that put every height of a unit's last m-tile on the GPU
+# GEMM: 1..64 rows (an M = 64 MMA) and 65..128 (M = 128), as the only m-tile,
+# the second of two, the third of a 3-m-tile unit and the last of a group of
+# a heavy expert (5 m-tiles: groups of 2, 2, 1; 7 m-tiles: 2, 2, 2, 1), plus
+# the edges 64/65, 192/193, 320/321, 448/449 and an empty expert.
+LAST_TILE_COUNTS = [1, 17, 64, 65, 100, 128, 129, 160, 192, 193, 250, 256, 257, 290, 320,
+                    321, 384, 400, 448, 449, 520, 0, 800]
+
+
+def routing_with_counts(counts, seed=0):
+    """top-1 routing [T, 1] in which expert e gets counts[e] tokens, shuffled."""
+    owner = np.repeat(np.arange(len(counts), dtype=np.int32), counts)
+    np.random.default_rng(seed).shuffle(owner)
+    return owner.reshape(-1, 1)

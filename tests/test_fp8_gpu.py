@@ -139,6 +139,14 @@ def test_fp8_gemm_skew_and_empty_experts(gpu_lib, gemm_kernel):
     _fp8_case(gpu_lib, c.x, c.topk, c.W, 16)
 
 
+def test_fp8_gemm_every_last_m_tile_height(gpu_lib, gemm_kernel):
+    from _gpu_util import LAST_TILE_COUNTS, routing_with_counts
+    topk = routing_with_counts(LAST_TILE_COUNTS, seed=22)
+    E, T = len(LAST_TILE_COUNTS), topk.shape[0]
+    c = ig.make_case(ig.custom(T=T, D=384, E=E, k=1, De=320, seed=22))
+    _fp8_case(gpu_lib, c.x, topk, c.W, E)
+
+
 def test_fp8_gemm_bad_perm_entry_sets_status(gpu_lib, gemm_kernel):
     pk = gpu_lib
     T, k, E, D, De = 64, 2, 4, 64, 64
@@ -260,13 +268,20 @@ def test_fp8_full_size_sampled(gpu_lib, name):
 
 
 @pytest.mark.parametrize("RT,K,E,k,N", [(512, 640, 4, 2, 576), (300, 208, 3, 1, 200),
-                                        (1000, 128, 2, 2, 256)])
+                                        (1000, 128, 2, 2, 256), (None, 256, None, 1, 200)])
 def test_fp8_grouped_gemm(gpu_lib, RT, K, E, k, N):
     """Down-projection on E4M3 codes: rows already in expert order (A's row
-    j is its own token, so the oracle's perm is the identity with k = 1)."""
+    j is its own token, so the oracle's perm is the identity with k = 1).
+    RT = None: experts with every height of the last m-tile."""
     pk = gpu_lib
+    topk = None
+    if RT is None:
+        from _gpu_util import LAST_TILE_COUNTS, routing_with_counts
+        topk = routing_with_counts(LAST_TILE_COUNTS, seed=23)
+        E, RT = len(LAST_TILE_COUNTS), topk.shape[0]
     wl = ig.custom(T=RT, D=K, E=E, k=k, De=N, seed=14)
-    topk = ig.make_topk(wl)
+    if topk is None:
+        topk = ig.make_topk(wl)
     _, offsets = oracle.route_counts(topk, E)
     R = RT * k
     A = ig.normal_bf16(14, 7, 0, R * K).reshape(R, K)

@@ -155,6 +155,16 @@ def test_grouped_gemm_all_rows(gpu_lib, T, K, E, k, N):
     _check_grouped(gpu_lib, A, offsets, W)
 
 
+def test_grouped_gemm_every_last_m_tile_height(gpu_lib):
+    from _gpu_util import LAST_TILE_COUNTS, routing_with_counts
+    topk = routing_with_counts(LAST_TILE_COUNTS, seed=24)
+    E, R = len(LAST_TILE_COUNTS), topk.shape[0]
+    _, offsets = oracle.route_counts(topk, E)
+    A = ig.normal_bf16(24, 7, 0, R * 256).reshape(R, 256)
+    W = ig.make_W(ig.custom(T=R, D=256, E=E, k=1, De=200, seed=24))
+    _check_grouped(gpu_lib, A, offsets, W)
+
+
 def test_grouped_gemm_down_projection_shape(gpu_lib):
     # the ep down-projection: K = D_expert = 2048, N = D = 7168, 256 experts
     from _gpu_util import boundary_rows

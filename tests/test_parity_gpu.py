@@ -49,6 +49,17 @@ def test_multi_tile_all_rows(gpu_lib, gemm_kernel, T, D, E, k, De):
     check_case(gpu_lib, x, topk, W, E)
 
 
+def test_every_last_m_tile_height(gpu_lib, gemm_kernel):
+    """Experts whose last m-tile holds 1..128 rows in every unit shape (a last
+    m-tile of at most 64 rows runs as an M = 64 MMA)."""
+    from _gpu_util import LAST_TILE_COUNTS, routing_with_counts
+    topk = routing_with_counts(LAST_TILE_COUNTS, seed=21)
+    E, T = len(LAST_TILE_COUNTS), topk.shape[0]
+    x, _, W = _case(T, 320, E, 1, 320, seed=21)
+    res, _ = check_case(gpu_lib, x, topk, W, E)
+    assert res["counts"].tolist() == LAST_TILE_COUNTS
+
+
 def test_single_token_single_expert(gpu_lib, gemm_kernel):
     x, topk, W = _case(1, 64, 1, 1, 64)
     check_case(gpu_lib, x, topk, W, 1)
