@@ -212,6 +212,9 @@ struct Unit {
     bool shared_w;  // other units of this expert load the same W tiles
 };
 
+// Sleep between tests of a wait that spans a whole unit (epilogue, scheduler).
+constexpr uint32_t IDLE_SLEEP_NS = 1024;
+
 // One lane waits; the warp learns the outcome.
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const volatile int* abort,
                                           uint64_t limit) {
@@ -829,7 +832,12 @@ __global__ void __launch_bounds__(THREADS, 1)
                     if (c * 32 < U.bn && col < De) cs_pre[c] = __ldg(sw_u + col);
                 }
             }
-            if (!warp_wait(acc_full, acc_phase, abort, limit)) {
+            bool acc_ok = true;
+            if (lane == 0)
+                acc_ok = mbar_wait_backoff(acc_full, acc_phase, abort, limit, IDLE_SLEEP_NS);
+            acc_ok = __shfl_sync(0xffffffffu, acc_ok ? 1 : 0, 0) != 0;
+            __syncwarp();
+            if (!acc_ok) {
                 if (lane == 0) fail(abort, status);
                 break;
             }
@@ -963,7 +971,8 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
             bool ok = true;
             if (lane == 0) {
-                ok = mbar_wait(qempty0 + 8 * qc.s, qc.ph ^ 1u, abort, limit);
+                ok = mbar_wait_backoff(qempty0 + 8 * qc.s, qc.ph ^ 1u, abort, limit,
+                                       IDLE_SLEEP_NS);
                 if (ok) {
 #pragma unroll
                     for (int i = 0; i < QWORDS; ++i) ctl->q[qc.s][i] = d[i];

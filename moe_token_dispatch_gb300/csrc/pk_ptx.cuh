@@ -96,6 +96,26 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const v
     }
 }
 
+// mbar_wait for waits that usually last many microseconds (a role idle for
+// a whole work unit): between tests the thread sleeps about sleep_ns, so that
+// the idle warps draw less power on a power-capped GPU. Same limits.
+__device__ __forceinline__ bool mbar_wait_backoff(uint32_t bar, uint32_t parity,
+                                                  const volatile int* abort, uint64_t limit_ns,
+                                                  uint32_t sleep_ns) {
+    if (mbar_test_parity(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    const long long c0 = clock64();
+    const long long cmax =
+        limit_ns < (1ull << 60) ? static_cast<long long>(limit_ns * 4) : (1ll << 62);
+    while (true) {
+        if (mbar_test_parity(bar, parity)) return true;
+        __nanosleep(sleep_ns);
+        if (abort && *abort) return false;
+        if (globaltimer_ns() - t0 > limit_ns) return false;
+        if (clock64() - c0 > cmax) return false;
+    }
+}
+
 // ------------------------------------------------------------------ TMA
 // Tiled 3-D load of one box into shared memory; completion is counted in
 // bytes on `bar`.
