@@ -30,12 +30,14 @@
 //              the expert offsets. Warps share an SM sub-partition with the
 //              warps whose index is equal mod 4; this keeps the busy gather
 //              warps off the MMA issuer's sub-partition.
-// Two rings of shared-memory slots connect producers and MMA: three 32 KiB W
-// slots and four 32 KiB A slots (m-tiles 0 and 1), one of each per K-step; a
-// 3-m-tile unit puts its m-tile 2 in the second half of its W slot (its W
-// tile is 16 KiB). The ring that bounds the K-loop is the gathered rows':
-// measured on ep, one A slot less costs 31 %, one W slot less nothing. So
-// the A ring runs four K-steps ahead and the W ring three. One full and one
+// Two rings of shared-memory slots connect producers and MMA: W slots and
+// A slots (m-tiles 0 and 1) of 32 KiB, one of each per K-step; a 3-m-tile
+// unit puts its m-tile 2 in the second half of its W slot (its W tile is
+// 16 KiB). When x is larger than L2 can keep beside the W stream, some
+// gathered rows come from DRAM, and the A ring needs the depth: three W and
+// four A slots (measured on ep: one A slot less costs 31 %, one W slot less
+// nothing). When x stays in L2, four W and three A slots hide more of the W
+// stream's HBM latency (decode, mid: 1.4-6 % faster). One full and one
 // empty barrier per K-step (a ring of eight pairs, indexed by K-step)
 // serve both rings: the full barrier counts the W bytes and every gather
 // thread's arrival, so the MMA thread waits once per K-step, and its one
@@ -94,25 +96,28 @@ constexpr int ROW_BYTES = 128;               // bytes of one row segment per sta
 constexpr int B_BOX = 64;                    // W box: 64 columns (bf16) or 64 rows (FP8 codes)
 constexpr int B_BOX_BYTES = B_BOX * ROW_BYTES;  // 8 KiB
 constexpr int A_BYTES = BM * BK * 2;         // 16 KiB per m-tile
-// Two rings, one slot per K-step each: the W ring runs up to four K-steps
-// ahead of the tensor cores (HBM latency), the A ring three (gathered rows).
-// A W slot holds the W tile (bn_max x 128 B); 3-m-tile units (bn_max = 128)
-// put their third A tile in its second half. An A slot holds m-tiles 0, 1.
-constexpr int W_STAGES = 3;
-constexpr int A_STAGES = 4;
+// Two rings, one slot per K-step each, seven 32 KiB slots in all: a W slot
+// holds the W tile (bn_max x 128 B; 3-m-tile units, bn_max = 128, put their
+// third A tile in its second half), an A slot m-tiles 0 and 1. The split is
+// a template parameter (kWDeep): three W + four A slots when the gathered
+// rows may miss L2 (x larger than L2 can keep beside the W stream: their
+// DRAM-latency tail needs the deeper A ring), four W + three A slots when x
+// stays in L2, so that the W ring hides more of HBM's latency.
+constexpr int SLOTS = 7;
 constexpr int W_SLOT = 32 * 1024;
 constexpr int A_SLOT = 2 * A_BYTES;
-constexpr int A_RING_OFF = W_STAGES * W_SLOT;                // 96 KiB
-constexpr int RING_BYTES = A_RING_OFF + A_STAGES * A_SLOT;   // 224 KiB
+static_assert(W_SLOT == A_SLOT, "one slot size for both rings");
+constexpr int RING_BYTES = SLOTS * W_SLOT;   // 224 KiB
+// x sizes (bytes) up to which the deep W ring is used
+constexpr int64_t DEEP_W_MAX_X_BYTES = int64_t{24} << 20;
 // K-step j uses full/empty barrier pair j mod NBAR. Each producer waits for
-// the K-step its slot's previous user ran (j - W_STAGES for a W slot and for
+// the K-step its slot's previous user ran (j - W slots for a W slot and for
 // m-tile 2 of a 3-m-tile unit, which lives in the W slot's second half;
-// j - A_STAGES for an A slot) before it arrives for K-step j. With more
+// j - A slots for an A slot) before it arrives for K-step j. With more
 // barrier pairs than either lag, the phase a producer waits for can never be
 // overtaken by the next phase of the same barrier, and no arrival can reach
 // a barrier whose previous phase is still open.
 constexpr int NBAR = 8;
-static_assert(NBAR > W_STAGES && NBAR > A_STAGES, "barrier ring shorter than a slot lag");
 constexpr int UMMA_K = 16;
 // A unit whose last m-tile holds at most 64 rows issues that m-tile's MMAs
 // with M = 64 (bf16 and FP8; not MX). An M = 64 MMA takes the tensor core as
@@ -353,7 +358,7 @@ __device__ __forceinline__ void scale_chunk(uint32_t (&v)[32], float rs, float c
 // along D: sx_ is the rows' scale bytes [T, D / 32], sw_ the weights' scale
 // pieces (1 KiB per 192-column tile and K-step); otherwise (FP8) both are
 // fp32 scales [T] and [E, De].
-template <bool kGather, bool kFp8, bool kMx = false>
+template <bool kGather, bool kFp8, bool kMx = false, bool kWDeep = false>
 __global__ void __launch_bounds__(THREADS, 1)
     k_dispatch_gemm(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap amap,
                     const uint8_t* __restrict__ x, const void* __restrict__ sx_,
@@ -362,6 +367,10 @@ __global__ void __launch_bounds__(THREADS, 1)
                     uint16_t* __restrict__ out, int32_t T, int32_t k, int32_t D, int32_t E,
                     int32_t De, int32_t* status, uint64_t limit, int64_t stall) {
     static_assert(!kMx || (kGather && kFp8), "MXFP8 is a form of the FP8 dispatch GEMM");
+    constexpr int WS = kWDeep ? 4 : 3;        // W slots
+    constexpr int AS = SLOTS - WS;            // A slots
+    constexpr int A_RING = WS * W_SLOT;       // the A ring follows the W ring
+    static_assert(NBAR > WS && NBAR > AS, "barrier ring shorter than a slot lag");
     const float* sx = static_cast<const float*>(sx_);
     const float* sw = static_cast<const float*>(sw_);
     extern __shared__ uint8_t smem_raw[];
@@ -384,7 +393,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     };
     // shared-memory address of m-tile mt of a K-step using W slot ws, A slot as
     auto a_tile = [&](int ws, int as, int mt) -> uint32_t {
-        return mt < 2 ? sbase + A_RING_OFF + as * A_SLOT + mt * A_BYTES
+        return mt < 2 ? sbase + A_RING + as * A_SLOT + mt * A_BYTES
                       : sbase + ws * W_SLOT + (W_SLOT - A_BYTES);
     };
 
@@ -436,8 +445,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         const uint64_t pol_x = policy_evict_last();  // rows are re-read by the unit's other n-tiles
         Cursor<NQ> qc;
         Cursor<NBAR> bc;
-        Cursor<A_STAGES> ac;
-        Cursor<NBAR> back = lag_cursor<A_STAGES>();  // the A slot's previous user
+        Cursor<AS> ac;
+        Cursor<NBAR> back = lag_cursor<AS>();  // the A slot's previous user
         bool ok = true, bad = false;
         while (ok) {
             Unit U;
@@ -474,7 +483,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 const int64_t koff = static_cast<int64_t>(ks) * ROW_BYTES;
 #pragma unroll
                 for (int mt = 0; mt < 2; ++mt) {
-                    const uint32_t dst0 = sbase + A_RING_OFF + ac.s * A_SLOT + mt * A_BYTES + rb * 128 + swz;
+                    const uint32_t dst0 = sbase + A_RING + ac.s * A_SLOT + mt * A_BYTES + rb * 128 + swz;
 #pragma unroll
                     for (int i = 0; i < ROWS_PER_THREAD; ++i)
                         if (src[mt][i])
@@ -500,8 +509,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int nbr = D / 32;                   // scale bytes per token row
         Cursor<NQ> qc;
         Cursor<NBAR> bc;
-        Cursor<W_STAGES> wc;
-        Cursor<NBAR> back = lag_cursor<W_STAGES>();  // the W slot's previous user
+        Cursor<WS> wc;
+        Cursor<NBAR> back = lag_cursor<WS>();  // the W slot's previous user
         bool ok = true, bad = false;
         while (ok) {
             Unit U;
@@ -548,7 +557,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     } else if (kGather && warp == GATHER2_WARP) {
         // -------------------------- dispatch, m-tile 2 of 3-m-tile units
         // Its own warp, so that its shorter lead (it writes the W slot's
-        // second half, whose previous user is W_STAGES K-steps back) does not
+        // second half, whose previous user is WS K-steps back) does not
         // hold back the arrivals of m-tiles 0 and 1, which a thread's
         // cp.async arrivals would otherwise cover together. Every K-step it
         // waits and arrives, also without rows to copy.
@@ -557,8 +566,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         const uint64_t pol_x = policy_evict_last();
         Cursor<NQ> qc;
         Cursor<NBAR> bc;
-        Cursor<W_STAGES> wc;
-        Cursor<NBAR> back = lag_cursor<W_STAGES>();  // the W slot's previous user
+        Cursor<WS> wc;
+        Cursor<NBAR> back = lag_cursor<WS>();  // the W slot's previous user
         bool ok = true, bad = false;
         while (ok) {
             Unit U;
@@ -619,11 +628,11 @@ __global__ void __launch_bounds__(THREADS, 1)
             const uint64_t pol_reuse = policy_evict_last();  // also A: re-read by every n-tile
             Cursor<NQ> qc;
             Cursor<NBAR> bc;
-            Cursor<W_STAGES> wc;
-            Cursor<A_STAGES> ac;
+            Cursor<WS> wc;
+            Cursor<AS> ac;
             // the W slot's previous user (grouped GEMM: also m-tile 2's slot; the
             // A slot's previous user is one K-step older still)
-            Cursor<NBAR> back = lag_cursor<W_STAGES>();
+            Cursor<NBAR> back = lag_cursor<WS>();
             uint32_t w_issued = 0, w_par = 0;
             bool ok = true;
             // Failure-detection test hook (off: stall < 0): CTA stall >> 40 arms
@@ -698,8 +707,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (lane == 0) {
             Cursor<NQ> qc;
             Cursor<NBAR> bc;
-            Cursor<W_STAGES> wc;
-            Cursor<A_STAGES> ac;
+            Cursor<WS> wc;
+            Cursor<AS> ac;
             uint32_t acc_phase = 0;
             bool ok = true;
             // Descriptors of shared-memory address 0 (the address field holds
@@ -746,7 +755,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                     fence_proxy_async_smem();
                     const uint64_t b_st = b_desc0 + ((sbase + wc.s * W_SLOT) >> 4);
                     // MX: this K-step's scales into TMEM buffer ac.s (its last
-                    // reader, the K-step A_STAGES back, has completed: the rows
+                    // reader, the K-step AS back, has completed: the rows
                     // of this K-step could only be gathered after it)
                     const uint32_t sft = tmem + MX_SF_TMEM + MX_SF_COLS * static_cast<uint32_t>(ac.s);
                     if (kMx) {
@@ -1097,6 +1106,15 @@ int launch_common(bool gather, bool fp8, const void* A, const void* sx, const in
                                      SMEM_BYTES) != cudaSuccess ||
                 cudaFuncSetAttribute(k_dispatch_gemm<true, true, true>,
                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     SMEM_BYTES) != cudaSuccess ||
+                cudaFuncSetAttribute(k_dispatch_gemm<true, false, false, true>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     SMEM_BYTES) != cudaSuccess ||
+                cudaFuncSetAttribute(k_dispatch_gemm<true, true, false, true>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     SMEM_BYTES) != cudaSuccess ||
+                cudaFuncSetAttribute(k_dispatch_gemm<true, true, true, true>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      SMEM_BYTES) != cudaSuccess)
                 return PK_ERR_CUDA;
             di.attr_set = true;
@@ -1124,8 +1142,16 @@ int launch_common(bool gather, bool fp8, const void* A, const void* sx, const in
             return PK_ERR_UNSUPPORTED;
     }
     const uint8_t* a8 = static_cast<const uint8_t*>(A);
-    if (mx)
+    // gathered rows that stay in L2 (x small): the deep W ring
+    const bool deep = gather && static_cast<int64_t>(T) * D * (fp8 ? 1 : 2) <= DEEP_W_MAX_X_BYTES;
+    if (mx && deep)
+        k_dispatch_gemm<true, true, true, true><<<sms, THREADS, SMEM_BYTES, stream>>>(
+            wmap, amap, a8, sx, sw, perm, offsets, out, T, k, D, E, De, status, wait_limit_ns, stall);
+    else if (mx)
         k_dispatch_gemm<true, true, true><<<sms, THREADS, SMEM_BYTES, stream>>>(
+            wmap, amap, a8, sx, sw, perm, offsets, out, T, k, D, E, De, status, wait_limit_ns, stall);
+    else if (fp8 && gather && deep)
+        k_dispatch_gemm<true, true, false, true><<<sms, THREADS, SMEM_BYTES, stream>>>(
             wmap, amap, a8, sx, sw, perm, offsets, out, T, k, D, E, De, status, wait_limit_ns, stall);
     else if (fp8 && gather)
         k_dispatch_gemm<true, true><<<sms, THREADS, SMEM_BYTES, stream>>>(
@@ -1133,6 +1159,10 @@ int launch_common(bool gather, bool fp8, const void* A, const void* sx, const in
     else if (fp8)
         k_dispatch_gemm<false, true><<<sms, THREADS, SMEM_BYTES, stream>>>(
             wmap, amap, a8, sx, sw, nullptr, offsets, out, T, k, D, E, De, status, wait_limit_ns, stall);
+    else if (gather && deep)
+        k_dispatch_gemm<true, false, false, true><<<sms, THREADS, SMEM_BYTES, stream>>>(
+            wmap, amap, a8, nullptr, nullptr, perm, offsets, out, T, k, D, E, De, status,
+            wait_limit_ns, stall);
     else if (gather)
         k_dispatch_gemm<true, false><<<sms, THREADS, SMEM_BYTES, stream>>>(
             wmap, amap, a8, nullptr, nullptr, perm, offsets, out, T, k, D, E, De, status,
