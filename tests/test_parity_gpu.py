@@ -207,19 +207,22 @@ def test_bounded_wait_times_out_and_context_survives(gpu_lib):
     check_case(pk, x, topk, W, 2)
 
 
-@pytest.mark.parametrize("grouped", [False, True])
-def test_gemm_pipeline_timeout_drains_every_role(gpu_lib, grouped):
+@pytest.mark.parametrize("grouped,big_x", [(False, False), (True, False), (False, True)])
+def test_gemm_pipeline_timeout_drains_every_role(gpu_lib, grouped, big_x):
     """A K-step whose copies are never issued (test hook on CTA 0) makes the
     MMA thread's bounded wait run out inside the real pipeline: the launch
     ends by itself with PK_ERR_TIMEOUT, every role has left its loop (the
     producers and dispatch warps are blocked on slots that the stalled K-step
     never frees, so they leave through the abort flag), TMEM was freed, and
-    the next launches on the same context run normally."""
+    the next launches on the same context run normally. big_x: x of 29 MB,
+    more than the 24 MiB up to which the dispatch GEMM runs four W slots, so
+    the launch takes the three-W-slot ring split."""
     pk = gpu_lib
     pk.pk_moe_set_gemm_kernel(pk.PK_GEMM_KERNEL_SINGLE)
     # 64 experts x 8 n-tiles of 256 columns, 8 K-steps each: CTA 0 owns several
     # units, so its producers fill the ring past the stalled K-step and block.
-    T, D, E, k, De = 256, 512, 64, 2, 2048
+    # big_x: 16 experts of 256 rows, 112 K-steps per unit (one unit per CTA).
+    T, D, E, k, De = (2048, 7168, 16, 2, 256) if big_x else (256, 512, 64, 2, 2048)
     x, topk, W = _case(T, D, E, k, De)
     Wd = u16_to_bf16_dev(W)
     md = pk.MoeDispatch(T, k, E, D, De)
