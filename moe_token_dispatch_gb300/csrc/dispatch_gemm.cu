@@ -7,8 +7,10 @@
 //
 // Persistent kernel, one CTA per SM, 12 warps:
 //   warps 0-3  epilogue: tcgen05.ld of the warp's TMEM lane quarter, bf16
-//              round-to-nearest-even, masked 16-byte stores of valid rows and
-//              columns.
+//              round-to-nearest-even, stores of the valid rows and columns
+//              (32-byte stores of eight rows x 128 B after a transpose inside
+//              each group of four lanes); between units the warps sleep
+//              between tests of the accumulator barrier.
 //   warp 4     MMA issuer (one thread) and TMEM owner: tcgen05.mma M=128 x
 //              N=bn x K=16 per m-tile (M=64 for a last m-tile of at most 64
 //              rows) into fp32 accumulators in TMEM; each commit frees a
@@ -61,6 +63,13 @@
 // epilogue multiplies each accumulator by its row's and column's scale (both
 // loaded into registers while the unit's MMAs still run, so that the
 // accumulators are not held in TMEM across those loads).
+//
+// With kMx (and kFp8) the codes carry one E8M0 scale per 32 elements along D
+// (MXFP8): units of at most two m-tiles and 192 columns, so that four
+// 16-column scale buffers fit in TMEM beside the accumulators; each K-step's
+// W scale piece follows its codes in the W slot, warp 11 gathers the rows'
+// scale bytes into the same slot, and the MMA thread copies both into TMEM
+// (tcgen05.cp) before the block-scaled MMAs (kind::mxf8f6f4).
 //
 // Work unit = (expert e, group of m-tiles, n-tile), with a shape chosen per
 // expert so that TMEM (512 fp32 columns x 128 lanes) holds every accumulator
