@@ -54,9 +54,38 @@ def load_peaks():
         return dict(PEAKS_FALLBACK), "fallback"
 
 
+def strip_comments(text: str) -> str:
+    """C/C++/CUDA source without its comments, whitespace runs collapsed: two
+    sources with the same code (comments or layout edited) give the same
+    text. String and character literals are kept as they are."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and text[j] != c:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            out.append(" ")
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
 def source_digest(path=GEMM_SOURCE) -> str:
-    with open(path, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+    """First 16 hex digits of the sha256 of a kernel source's code (comments
+    and whitespace removed): the fingerprint an ncu summary records of the
+    code it was captured on."""
+    with open(path, encoding="utf-8") as f:
+        return hashlib.sha256(strip_comments(f.read()).encode()).hexdigest()[:16]
 
 
 # Workloads too large for a full ncu capture take the DRAM traffic of a smaller
@@ -84,7 +113,7 @@ def profiled_traffic(workload: str, kernel: str = "single", prefix: str | None =
     except OSError:
         return None
     m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
-    s = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", text)
+    s = re.search(r"kernel_code_sha256_16:\s*([0-9a-f]+)", text)
     src_path = os.path.join(ROOT, "moe_token_dispatch_gb300", "csrc", src)
     if not m or not s or s.group(1) != source_digest(src_path):
         return None

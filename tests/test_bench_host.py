@@ -73,21 +73,24 @@ def test_reference_arm_line(capsys):
 
 def test_profiled_traffic_follows_the_kernel_source(tmp_path, monkeypatch):
     """traffic comes from profiles/<prefix>_<workload>.md (else its smaller
-    stand-in, scaled) only while the recorded source hash matches."""
+    stand-in, scaled) only while the recorded code fingerprint matches: an
+    edit of comments or layout keeps it, a change of code drops it."""
     prof = tmp_path / "profiles"
     src_dir = tmp_path / "moe_token_dispatch_gb300" / "csrc"
     prof.mkdir()
     src_dir.mkdir(parents=True)
-    (src_dir / "k.cu").write_text("kernel v1\n")
+    (src_dir / "k.cu").write_text("kernel v1;\n")
     digest = bench.source_digest(str(src_dir / "k.cu"))
-    (prof / "kk_ep32.md").write_text(f"kernel_source_sha256_16: {digest}\n"
+    (prof / "kk_ep32.md").write_text(f"kernel_code_sha256_16: {digest}\n"
                                      "traffic_bytes_per_launch: 1.0e+09\n")
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
     assert bench.profiled_traffic("ep", prefix="kk", src="k.cu") == 1.0e9 * 256 / 32
-    (prof / "kk_ep.md").write_text(f"kernel_source_sha256_16: {digest}\n"
+    (prof / "kk_ep.md").write_text(f"kernel_code_sha256_16: {digest}\n"
                                    "traffic_bytes_per_launch: 3.0e+09\n")
     assert bench.profiled_traffic("ep", prefix="kk", src="k.cu") == 3.0e9   # direct capture wins
-    (src_dir / "k.cu").write_text("kernel v2\n")                             # source changed
+    (src_dir / "k.cu").write_text("// a note\nkernel   v1; /* more */\n")   # comments only
+    assert bench.profiled_traffic("ep", prefix="kk", src="k.cu") == 3.0e9
+    (src_dir / "k.cu").write_text("kernel v2;\n")                           # code changed
     assert bench.profiled_traffic("ep", prefix="kk", src="k.cu") is None
 
 
@@ -99,9 +102,16 @@ def test_committed_profiles_carry_hash_and_traffic():
         if name == "launches_ep.md":
             continue
         text = open(os.path.join(pdir, name)).read()
-        assert re.search(r"kernel_source_sha256_16: [0-9a-f]{16}", text), name
+        assert re.search(r"kernel_code_sha256_16: [0-9a-f]{16}", text), name
         assert re.search(r"traffic_bytes_per_launch: [0-9.eE+]+", text), name
         assert "ncu " in text and "--clock-control none" in text, name
+
+
+def test_code_fingerprint_ignores_comments_not_strings():
+    a = 'asm("mov.u32 %0, 1; // not a comment"); int x = 1; // note\n/* block */ char c = \'/\';'
+    b = 'asm("mov.u32 %0, 1; // not a comment");\n  int x = 1;\n char c = \'/\';'
+    assert bench.strip_comments(a) == bench.strip_comments(b)
+    assert bench.strip_comments(a) != bench.strip_comments(a.replace("1; //", "2; //"))
 
 
 def test_binding_roofline_picks_the_slower_limit():
