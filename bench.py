@@ -564,6 +564,8 @@ def measure_other(args, wl, head_wl, head_x, head_W, dev, stream, peaks, peak_ki
         "value": flops / (step_ms * 1e-3) / 1e12, "unit": UNIT,
         "pct_bf16_peak": 100.0 * flops / (step_ms * 1e-3) / 1e12 / peaks["bf16_tflops"],
         "roofline": dict(roof, peak_kind=peak_kind, kernel="k_dispatch_gemm",
+                         traffic=profiled_traffic(
+                             wl.name, "pair" if args.gemm_kernel == "pair" else "single"),
                          algorithmic_bytes=alg_bytes, flops=flops, bytes_breakdown=b),
         "cpu_baseline": {"value": cpu_value, "unit": UNIT, "cores": os.cpu_count() or 1,
                          "kind": "oracle",
