@@ -50,9 +50,12 @@
 //
 // The same kernel, instantiated with kGather = false, is the grouped GEMM of
 // rows that are already in expert order (the down-projection that follows the
-// expert MLP: out2[j, :] = h[j, :] @ W2[e(j)]): the W producer then also
-// TMA-loads each m-tile of A as one 128-row box, and the gather warps idle
-// (with kFp8 too: E4M3 codes of h with one scale per row).
+// expert MLP: out2[j, :] = h[j, :] @ W2[e(j)]): each m-tile of A arrives by
+// TMA as one 128-row box, m-tiles 0 and 1 from an A producer of their own
+// (warp 6, lane 0) and m-tile 2 with W, and the other gather warps idle (with
+// kFp8 too: E4M3 codes of h with one scale per row). It always runs four W
+// and three A slots: an expert's A rows are re-read by its concurrent n-tiles
+// from L2, and the W stream gains the deeper ring (ep 1.683 -> 1.604 ms).
 //
 // With kFp8, the same pipeline is the FP8 variant of the expert GEMM: x and W
 // arrive as E4M3 codes with one fp32 scale per token row and per (expert,
@@ -380,6 +383,13 @@ __global__ void __launch_bounds__(THREADS, 1)
     constexpr int AS = SLOTS - WS;            // A slots
     constexpr int A_RING = WS * W_SLOT;       // the A ring follows the W ring
     static_assert(NBAR > WS && NBAR > AS, "barrier ring shorter than a slot lag");
+    // Grouped GEMM (rows already in expert order, A by TMA) with the deep W
+    // ring: the W producer can no longer load A too (it waits for its W
+    // slot's previous user, WS K-steps back, but an A slot's previous user is
+    // only AS < WS back), so an A producer of its own (warp 6, lane 0) loads
+    // m-tiles 0 and 1; the W producer loads W and m-tile 2, which lives in
+    // the W slot.
+    constexpr bool kSplitA = !kGather && kWDeep;
     const float* sx = static_cast<const float*>(sx_);
     const float* sw = static_cast<const float*>(sw_);
     extern __shared__ uint8_t smem_raw[];
@@ -417,7 +427,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < NBAR; ++s) {
-            mbar_init(wfull0 + 8 * s, kGather ? 1 + GATHER_THREADS + 32 : 1);
+            mbar_init(wfull0 + 8 * s, kGather ? 1 + GATHER_THREADS + 32 : (kSplitA ? 2 : 1));
             mbar_init(wempty0 + 8 * s, 1);
         }
         mbar_init(acc_full, 1);
@@ -425,7 +435,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         mbar_init(drain, 1);
         for (int s = 0; s < NQ; ++s) {
             mbar_init(qfull0 + 8 * s, 1);
-            mbar_init(qempty0 + 8 * s, (kGather ? GATHER_WARPS + 1 : 0) + 2 + EPI_WARPS);
+            mbar_init(qempty0 + 8 * s,
+                      (kGather ? GATHER_WARPS + 1 : 0) + (kSplitA ? 1 : 0) + 2 + EPI_WARPS);
         }
         ctl->abort = 0;
         fence_barrier_init();
@@ -630,6 +641,53 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         cp_async_wait_all();
         if (bad) report(status, PK_ERR_BAD_INDEX);
+    } else if (kSplitA && warp == 6) {
+        // ---------------------------- A producer (grouped GEMM, deep W ring)
+        if (lane == 0) {
+            const uint64_t pol_reuse = policy_evict_last();  // re-read by every n-tile
+            Cursor<NQ> qc;
+            Cursor<NBAR> bc;
+            Cursor<AS> ac;
+            Cursor<NBAR> back = lag_cursor<AS>();  // the A slot's previous user
+            uint32_t a_issued = 0, a_par = 0;
+            bool ok = true;
+            while (ok) {
+                Unit U;
+                const int got = q_pop<false>(qfull0, qempty0, ctl->q, qc, U, abort, limit);
+                if (got <= 0) {
+                    if (got < 0) fail(abort, status);
+                    break;
+                }
+                const int a_lo = U.mpu < 2 ? U.mpu : 2;
+                for (int ks = 0; ks < nk; ++ks) {
+                    if (!mbar_wait(wempty0 + 8 * back.s, back.ph, abort, limit)) {
+                        fail(abort, status);
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t full = wfull0 + 8 * bc.s;
+                    mbar_arrive_expect_tx(full, static_cast<uint32_t>(a_lo * A_BYTES));
+                    // rows past the expert's end are loaded but never stored
+                    for (int mt = 0; mt < a_lo; ++mt)
+                        tma_load_2d(sbase + A_RING + ac.s * A_SLOT + mt * A_BYTES, &amap, ks * BKE,
+                                    U.row0 + mt * BM, full, pol_reuse);
+                    a_issued |= 1u << bc.s;
+                    a_par = (a_par & ~(1u << bc.s)) | (bc.ph << bc.s);
+                    bc.next();
+                    ac.next();
+                    back.next();
+                }
+            }
+            // Every copy this thread started must land before the CTA may exit
+            // (after an abort a barrier may lack the W producer's bytes: the
+            // first wait that runs out ends the drain, the copies have landed
+            // long before).
+            bool drained = true;
+            for (int s = 0; s < NBAR && drained; ++s)
+                if ((a_issued >> s) & 1u)
+                    drained = mbar_wait(wfull0 + 8 * s, (a_par >> s) & 1u, nullptr, limit);
+        }
+        __syncwarp();
     } else if (warp == W_WARP) {
         // ----------------------------------------------------- W producer
         if (lane == 0) {
@@ -672,7 +730,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                         break;
                     }
                     const uint32_t wfull = wfull0 + 8 * bc.s;
-                    mbar_arrive_expect_tx(wfull, kGather ? wtx : wtx + atx);
+                    mbar_arrive_expect_tx(wfull, (kGather || kSplitA) ? wtx : wtx + atx);
                     const uint32_t wsl = sbase + wc.s * W_SLOT;
                     const bool stalled = kcount++ == stall_step;
                     for (int b = 0; b < nbox && !stalled; ++b) {
@@ -696,7 +754,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                         w_par = (w_par & ~(1u << bc.s)) | (bc.ph << bc.s);
                     }
                     if (!kGather && !stalled) {  // rows past the expert's end are loaded but never stored
-                        for (int mt = 0; mt < U.mpu; ++mt)
+                        for (int mt = kSplitA ? 2 : 0; mt < U.mpu; ++mt)
                             tma_load_2d(a_tile(wc.s, ac.s, mt), &amap, ks * BKE, U.row0 + mt * BM,
                                         wfull, pol_reuse);
                     }
@@ -706,9 +764,12 @@ __global__ void __launch_bounds__(THREADS, 1)
                     back.next();
                 }
             }
-            // Every copy this thread started must land before the CTA may exit.
-            for (int s = 0; s < NBAR; ++s)
-                if ((w_issued >> s) & 1u) mbar_wait(wfull0 + 8 * s, (w_par >> s) & 1u, nullptr, limit);
+            // Every copy this thread started must land before the CTA may exit
+            // (the first wait that runs out ends the drain: see the A producer).
+            bool drained = true;
+            for (int s = 0; s < NBAR && drained; ++s)
+                if ((w_issued >> s) & 1u)
+                    drained = mbar_wait(wfull0 + 8 * s, (w_par >> s) & 1u, nullptr, limit);
         }
         __syncwarp();
     } else if (warp == MMA_WARP) {
@@ -1124,6 +1185,12 @@ int launch_common(bool gather, bool fp8, const void* A, const void* sx, const in
                                      SMEM_BYTES) != cudaSuccess ||
                 cudaFuncSetAttribute(k_dispatch_gemm<true, true, true, true>,
                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     SMEM_BYTES) != cudaSuccess ||
+                cudaFuncSetAttribute(k_dispatch_gemm<false, false, false, true>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     SMEM_BYTES) != cudaSuccess ||
+                cudaFuncSetAttribute(k_dispatch_gemm<false, true, false, true>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      SMEM_BYTES) != cudaSuccess)
                 return PK_ERR_CUDA;
             di.attr_set = true;
@@ -1166,7 +1233,7 @@ int launch_common(bool gather, bool fp8, const void* A, const void* sx, const in
         k_dispatch_gemm<true, true><<<sms, THREADS, SMEM_BYTES, stream>>>(
             wmap, amap, a8, sx, sw, perm, offsets, out, T, k, D, E, De, status, wait_limit_ns, stall);
     else if (fp8)
-        k_dispatch_gemm<false, true><<<sms, THREADS, SMEM_BYTES, stream>>>(
+        k_dispatch_gemm<false, true, false, true><<<sms, THREADS, SMEM_BYTES, stream>>>(
             wmap, amap, a8, sx, sw, nullptr, offsets, out, T, k, D, E, De, status, wait_limit_ns, stall);
     else if (gather && deep)
         k_dispatch_gemm<true, false, false, true><<<sms, THREADS, SMEM_BYTES, stream>>>(
@@ -1177,7 +1244,7 @@ int launch_common(bool gather, bool fp8, const void* A, const void* sx, const in
             wmap, amap, a8, nullptr, nullptr, perm, offsets, out, T, k, D, E, De, status,
             wait_limit_ns, stall);
     else
-        k_dispatch_gemm<false, false><<<sms, THREADS, SMEM_BYTES, stream>>>(
+        k_dispatch_gemm<false, false, false, true><<<sms, THREADS, SMEM_BYTES, stream>>>(
             wmap, amap, a8, nullptr, nullptr, perm, offsets, out, T, k, D, E, De, status,
             wait_limit_ns, stall);
     return cudaGetLastError() == cudaSuccess ? PK_OK : PK_ERR_CUDA;
