@@ -1162,37 +1162,20 @@ int launch_common(bool gather, bool fp8, const void* A, const void* sx, const in
         if (!di.attr_set) {
             if (cudaDeviceGetAttribute(&di.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
                 return PK_ERR_CUDA;
-            if (cudaFuncSetAttribute(k_dispatch_gemm<true, false>,
-                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     SMEM_BYTES) != cudaSuccess ||
-                cudaFuncSetAttribute(k_dispatch_gemm<false, false>,
-                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     SMEM_BYTES) != cudaSuccess ||
-                cudaFuncSetAttribute(k_dispatch_gemm<true, true>,
-                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     SMEM_BYTES) != cudaSuccess ||
-                cudaFuncSetAttribute(k_dispatch_gemm<false, true>,
-                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     SMEM_BYTES) != cudaSuccess ||
-                cudaFuncSetAttribute(k_dispatch_gemm<true, true, true>,
-                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     SMEM_BYTES) != cudaSuccess ||
-                cudaFuncSetAttribute(k_dispatch_gemm<true, false, false, true>,
-                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     SMEM_BYTES) != cudaSuccess ||
-                cudaFuncSetAttribute(k_dispatch_gemm<true, true, false, true>,
-                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     SMEM_BYTES) != cudaSuccess ||
-                cudaFuncSetAttribute(k_dispatch_gemm<true, true, true, true>,
-                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     SMEM_BYTES) != cudaSuccess ||
-                cudaFuncSetAttribute(k_dispatch_gemm<false, false, false, true>,
-                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     SMEM_BYTES) != cudaSuccess ||
-                cudaFuncSetAttribute(k_dispatch_gemm<false, true, false, true>,
-                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     SMEM_BYTES) != cudaSuccess)
-                return PK_ERR_CUDA;
+            // every instantiation launch_common can launch
+            const void* kernels[] = {
+                reinterpret_cast<const void*>(k_dispatch_gemm<true, false>),
+                reinterpret_cast<const void*>(k_dispatch_gemm<true, false, false, true>),
+                reinterpret_cast<const void*>(k_dispatch_gemm<true, true>),
+                reinterpret_cast<const void*>(k_dispatch_gemm<true, true, false, true>),
+                reinterpret_cast<const void*>(k_dispatch_gemm<true, true, true>),
+                reinterpret_cast<const void*>(k_dispatch_gemm<true, true, true, true>),
+                reinterpret_cast<const void*>(k_dispatch_gemm<false, false, false, true>),
+                reinterpret_cast<const void*>(k_dispatch_gemm<false, true, false, true>)};
+            for (const void* kern : kernels)
+                if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         SMEM_BYTES) != cudaSuccess)
+                    return PK_ERR_CUDA;
             di.attr_set = true;
         }
         sms = di.sms;
