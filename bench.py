@@ -746,12 +746,17 @@ def run_op(args, wl):
 
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
-    ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=1000)
-    ap.add_argument("--warmup", type=int, default=20)
-    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="ep")
-    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--gpus", type=int, default=1,
+                    help="GPUs (one process each, launched by torchrun when > 1); "
+                         "every rank runs its own replica")
+    ap.add_argument("--steps", type=int, default=1000, help="timed steps")
+    ap.add_argument("--warmup", type=int, default=20, help="untimed steps before them (at least 3)")
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours",
+                    help="ours: the CUDA path; reference: the CPU oracle on a bounded sample")
+    ap.add_argument("--workload", default="ep",
+                    help="tiny, mid, ep, skew, decode, or the profiling cuts ep32, decode32, skew32")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0,
+                    help="oracle CPU sample of the headline workload (cpu_baseline)")
     ap.add_argument("--cpu-seconds-other", type=float, default=3.0,
                     help="oracle CPU sample per additional workload")
     ap.add_argument("--no-others", action="store_true",
