@@ -750,7 +750,8 @@ def main(argv=None):
                     help="GPUs (one process each, launched by torchrun when > 1); "
                          "every rank runs its own replica")
     ap.add_argument("--steps", type=int, default=1000, help="timed steps")
-    ap.add_argument("--warmup", type=int, default=20, help="untimed steps before them (raised to 3 if fewer)")
+    ap.add_argument("--warmup", type=int, default=20,
+                    help="untimed steps before them (raised to 3 if fewer)")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours",
                     help="ours: the CUDA path; reference: the CPU oracle on a bounded sample")
     ap.add_argument("--workload", default="ep",
